@@ -1,0 +1,67 @@
+"""Planted mistakes in the oracle must be caught by its pins (CPU only).
+
+Each case copies attn_oracle.c, plants one plausible mistake by a textual
+edit, compiles the mutant with gcc into a temporary directory, points the
+oracle wrapper at it and runs every pin in test_oracle_pins.py.  At least one
+pin must fail for every mutant; the committed oracle itself is never touched.
+"""
+import ctypes
+import inspect
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_oracle.c")
+
+MUTANTS = {
+    "causal_excludes_diagonal": ("if (j > i) { s[j] = -INFINITY; continue; }",
+                                 "if (j >= i) { s[j] = -INFINITY; continue; }"),
+    "gqa_interleaved": ("const uint32_t kvh = h / heads_per_kv;",
+                        "const uint32_t kvh = h % num_kv_heads;"),
+    "decode_gqa_interleaved": ("const uint32_t kvh = h / repeat;",
+                               "const uint32_t kvh = h % kv_heads;"),
+    "prefill_scale_dropped": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "decode_scale_dropped": ("s[t] = scale * dot;", "s[t] = dot;"),
+    "window_start_off_by_one": ("total_seq - window : 0;", "total_seq - window + 1 : 0;"),
+    "mask_added_not_replaced": ("if (t < ws) s[t] = -1.0e4;", "if (t < ws) s[t] += -1.0e4;"),
+    "key_row_transposed": ("const float *kj = k + (size_t)j * kv_stride",
+                           "const float *kj = k + (size_t)i * kv_stride"),
+    "value_row_reversed": ("const float *vr = v + j * v_row_pitch;",
+                           "const float *vr = v + (n - 1 - j) * v_row_pitch;"),
+    "not_normalised": ("for (size_t j = 0; j < n; ++j) scores[j] /= l;", ""),
+    "exp_base_two": ("exp(scores[j] - m)", "exp2(scores[j] - m)"),
+    "append_wrong_row": ("+ position) * d + e;", "+ position - (position > 0)) * d + e;"),
+}
+
+
+def _pin_functions():
+    return [f for n, f in inspect.getmembers(pins, inspect.isfunction)
+            if n.startswith("test_")]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mut_src = tmp_path / "attn_oracle_mut.c"
+    mut_src.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                    str(mut_src), "-o", str(so), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_LIB_PATH", str(so))
+    monkeypatch.setattr(oracle, "build", lambda force=False: str(so))
+    monkeypatch.setattr(oracle, "_lib", None)
+    caught = []
+    for f in _pin_functions():
+        try:
+            f()
+        except (AssertionError, ValueError, FloatingPointError) as e:
+            caught.append(f.__name__)
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert caught, f"no pin caught the planted mistake {name}"
