@@ -1,0 +1,68 @@
+// attn_internal.h -- host-side declarations shared by the library's
+// translation units (not part of the public C ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Device status word bits (set by kernels with atomicOr).
+enum : unsigned int {
+    kStatusTimeout = 1u,  // a bounded mbarrier wait gave up
+    kStatusRange = 2u,    // an fp32 -> fp16 conversion overflowed
+};
+
+// Address of the device status word on the current device.
+unsigned int* device_status_ptr();
+
+// Number of SMs of the current device (152 when no device is visible).
+int device_sm_count();
+
+// Record a CUDA error for attn_last_error_string() and map it to a status.
+attn_status_t record_cuda_error(cudaError_t err);
+
+// ---------------------------------------------------------------- decode
+struct DecodePlan {
+    uint32_t window_start;
+    uint32_t rows_live;
+    uint32_t chunk;      // live rows per split
+    uint32_t n_splits;   // splits per KV head
+    uint32_t n_hgroups;  // query-head groups of <= 8 heads per KV head
+    size_t part_o_floats;
+    size_t part_ml_floats;
+    size_t workspace_bytes;
+};
+DecodePlan make_decode_plan(uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
+                            uint32_t total_seq, uint32_t window, int sm_count);
+
+cudaError_t launch_decode(const float* q, const float* k_cache, const float* v_cache,
+                          float* out, uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
+                          uint32_t max_seq, uint32_t total_seq, const DecodePlan& plan,
+                          float scale, float* part_o, float* part_ml, cudaStream_t stream);
+
+cudaError_t launch_kv_append(const float* k_src, const float* v_src, float* k_cache,
+                             float* v_cache, uint32_t kv_heads, uint32_t head_dim,
+                             uint32_t max_seq, uint32_t position, cudaStream_t stream);
+
+// ---------------------------------------------------------------- prefill
+cudaError_t launch_prefill_fp32(const float* q, const float* k, const float* v, float* o,
+                                uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
+                                float scale, cudaStream_t stream);
+
+size_t prefill_tc_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                  uint32_t head_dim);
+
+// Returns cudaErrorNotSupported when the tensor-map encoder is unavailable.
+cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, float* o,
+                              uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                              uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
+                              float scale, bool bf16, void* workspace, unsigned int* status,
+                              uint64_t wait_limit_ns, cudaStream_t stream);
+
+cudaError_t launch_wait_timeout_selftest(unsigned int* status, uint64_t limit_ns);
+
+}  // namespace attn

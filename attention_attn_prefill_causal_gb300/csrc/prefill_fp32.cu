@@ -1,0 +1,245 @@
+// prefill_fp32.cu -- exact-mode causal grouped-query prefill on CUDA cores,
+// fp32 throughout.
+//
+// Operation ("aprender-gpu 0.32.0 -- prefill_fused.rs", module doc,
+// Algorithm 1-3): query head h reads KV head h / heads_per_kv; row i attends
+// to keys j <= i with scores scale * Q[i].K[j], an online softmax (running
+// max, correction, p = exp(s - max)), O = O * corr + p V[j], and O / l at the
+// end.  Q/O rows use q_stride, K/V rows use kv_stride (packed layout).
+//
+// The page runs one warp per query head, walking all M rows serially and
+// reading K/V through L2.  Here a CTA takes 64 query rows of one head and
+// walks 64-key tiles staged in shared memory, so each K/V row is read from
+// global memory once per 64 query rows instead of once per row:
+//  * a warp owns 8 query rows and works on 4 of them at once, each lane
+//    scoring one key of a 32-key slice (dot product over head_dim from
+//    shared memory: a 128-bit K read per lane, a broadcast Q read);
+//  * per row, the slice's max and sum come from warp shuffles; the online
+//    softmax runs in base 2 (scores pre-multiplied by log2 e, as the page
+//    does before ex2);
+//  * for PV each lane owns head_dim/32 output elements and takes the
+//    slice's weights by shuffle.
+// Causal masking is the loop bound plus a per-key test on the diagonal tile.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 64;           // query rows per CTA
+constexpr int kBN = 64;           // keys per tile
+constexpr int kThreads = 256;     // 8 warps
+constexpr int kRowsPerWarp = kBM / (kThreads / 32);
+constexpr int kRowGroup = 4;      // rows a warp scores together
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Smem {
+    static constexpr int kPitch = D + 4;  // pad: 128-bit reads across rows hit distinct banks
+    float q[kBM][kPitch];
+    float k[kBN][kPitch];
+    float v[kBN][D];
+};
+
+template <int D>
+__device__ __forceinline__ void load_tile(float (*dst)[D + 4], const float* __restrict__ src,
+                                          uint32_t row0, uint32_t m, uint32_t stride,
+                                          uint32_t col0, int rows) {
+    constexpr int C4 = D / 4;
+    for (int t = threadIdx.x; t < rows * C4; t += kThreads) {
+        const int r = t / C4, c = (t % C4) * 4;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row0 + r < m)
+            val = *reinterpret_cast<const float4*>(src + (size_t)(row0 + r) * stride + col0 + c);
+        *reinterpret_cast<float4*>(&dst[r][c]) = val;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void load_v_tile(float (*dst)[D], const float* __restrict__ src,
+                                            uint32_t row0, uint32_t m, uint32_t stride,
+                                            uint32_t col0) {
+    constexpr int C4 = D / 4;
+    for (int t = threadIdx.x; t < kBN * C4; t += kThreads) {
+        const int r = t / C4, c = (t % C4) * 4;
+        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row0 + r < m)
+            val = *reinterpret_cast<const float4*>(src + (size_t)(row0 + r) * stride + col0 + c);
+        *reinterpret_cast<float4*>(&dst[r][c]) = val;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2)
+prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                    const float* __restrict__ v, float* __restrict__ o, uint32_t m,
+                    uint32_t heads_per_kv, uint32_t q_stride, uint32_t kv_stride,
+                    float scale_log2) {
+    constexpr int VEC = D / 32;  // output elements per lane
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t nqb = (m + kBM - 1) / kBM;
+    const uint32_t qb = nqb - 1 - blockIdx.x;  // longest causal extent first
+    const uint32_t h = blockIdx.y;
+    const uint32_t kvh = h / heads_per_kv;
+    const uint32_t q0 = qb * kBM;
+
+    load_tile<D>(sm.q, q, q0, m, q_stride, h * D, kBM);
+
+    float mrow[kRowsPerWarp], lrow[kRowsPerWarp], acc[kRowsPerWarp][VEC];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        mrow[r] = -CUDART_INF_F;
+        lrow[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[r][e] = 0.f;
+    }
+    const int wr0 = warp * kRowsPerWarp;        // first local row of this warp
+    const uint32_t last_row = min(q0 + kBM, m) - 1;
+    const uint32_t n_tiles = last_row / kBN + 1;
+
+    for (uint32_t t = 0; t < n_tiles; ++t) {
+        const uint32_t k0 = t * kBN;
+        __syncthreads();
+        load_tile<D>(sm.k, k, k0, m, kv_stride, kvh * D, kBN);
+        load_v_tile<D>(sm.v, v, k0, m, kv_stride, kvh * D);
+        __syncthreads();
+#pragma unroll
+        for (int grp = 0; grp < kRowsPerWarp / kRowGroup; ++grp) {
+            const int lr0 = wr0 + grp * kRowGroup;           // local row of the group
+            const uint32_t grow_last = q0 + lr0 + kRowGroup - 1;
+#pragma unroll
+            for (int half = 0; half < kBN / 32; ++half) {
+                const uint32_t key0 = k0 + half * 32;
+                if (key0 > grow_last) continue;              // whole slice above the diagonal
+                const int kl = half * 32 + lane;             // this lane's key (local)
+                const uint32_t key = k0 + kl;
+                float s[kRowGroup];
+#pragma unroll
+                for (int r = 0; r < kRowGroup; ++r) s[r] = 0.f;
+#pragma unroll 8
+                for (int d4 = 0; d4 < D / 4; ++d4) {
+                    const float4 kk = *reinterpret_cast<const float4*>(&sm.k[kl][d4 * 4]);
+#pragma unroll
+                    for (int r = 0; r < kRowGroup; ++r) {
+                        const float4 qq = *reinterpret_cast<const float4*>(&sm.q[lr0 + r][d4 * 4]);
+                        s[r] = fmaf(qq.x, kk.x, s[r]);
+                        s[r] = fmaf(qq.y, kk.y, s[r]);
+                        s[r] = fmaf(qq.z, kk.z, s[r]);
+                        s[r] = fmaf(qq.w, kk.w, s[r]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < kRowGroup; ++r) {
+                    const int ri = grp * kRowGroup + r;
+                    const uint32_t row = q0 + lr0 + r;
+                    float sc = (key <= row) ? s[r] * scale_log2 : -CUDART_INF_F;
+                    float mx = sc;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    const float m_new = fmaxf(mrow[ri], mx);
+                    if (m_new == -CUDART_INF_F) { s[r] = 0.f; continue; }  // nothing attended yet
+                    const float corr = exp2f(mrow[ri] - m_new);
+                    const float p = exp2f(sc - m_new);
+                    float ps = p;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        ps += __shfl_xor_sync(0xffffffffu, ps, off);
+                    lrow[ri] = fmaf(lrow[ri], corr, ps);
+                    mrow[ri] = m_new;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[ri][e] *= corr;
+                    s[r] = p;
+                }
+                // PV over the 32 keys of the slice
+#pragma unroll 4
+                for (int j = 0; j < 32; ++j) {
+                    const float* vrow = &sm.v[half * 32 + j][lane * VEC];
+                    float vv[VEC];
+                    if constexpr (VEC == 4) {
+                        const float4 t4 = *reinterpret_cast<const float4*>(vrow);
+                        vv[0] = t4.x; vv[1] = t4.y; vv[2] = t4.z; vv[3] = t4.w;
+                    } else if constexpr (VEC == 2) {
+                        const float2 t2 = *reinterpret_cast<const float2*>(vrow);
+                        vv[0] = t2.x; vv[1] = t2.y;
+                    } else {
+                        vv[0] = vrow[0];
+                    }
+#pragma unroll
+                    for (int r = 0; r < kRowGroup; ++r) {
+                        const float pj = __shfl_sync(0xffffffffu, s[r], j);
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            acc[grp * kRowGroup + r][e] = fmaf(pj, vv[e], acc[grp * kRowGroup + r][e]);
+                    }
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        const uint32_t row = q0 + wr0 + r;
+        if (row >= m) continue;
+        float* dst = o + (size_t)row * q_stride + h * D + lane * VEC;
+        const float inv_l = 1.0f / lrow[r];
+        if constexpr (VEC == 4) {
+            *reinterpret_cast<float4*>(dst) =
+                make_float4(acc[r][0] * inv_l, acc[r][1] * inv_l, acc[r][2] * inv_l, acc[r][3] * inv_l);
+        } else if constexpr (VEC == 2) {
+            *reinterpret_cast<float2*>(dst) = make_float2(acc[r][0] * inv_l, acc[r][1] * inv_l);
+        } else {
+            dst[0] = acc[r][0] * inv_l;
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const float* q, const float* k, const float* v, float* o, uint32_t m,
+                     uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
+                     uint32_t kv_stride, float scale, cudaStream_t stream) {
+    const int smem = (int)sizeof(Smem<D>);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_fp32_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid((m + kBM - 1) / kBM, num_q_heads);
+    prefill_fp32_kernel<D><<<grid, kThreads, smem, stream>>>(
+        q, k, v, o, m, num_q_heads / num_kv_heads, q_stride, kv_stride, scale * kLog2e);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_fp32(const float* q, const float* k, const float* v, float* o,
+                                uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
+                                float scale, cudaStream_t stream) {
+    switch (head_dim) {
+        case 32:
+            return launch_d<32>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
+                                scale, stream);
+        case 64:
+            return launch_d<64>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
+                                scale, stream);
+        case 128:
+            return launch_d<128>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
+                                 scale, stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace attn

@@ -1,0 +1,555 @@
+// prefill_tc.cu -- causal grouped-query prefill on the Blackwell tensor cores
+// (tcgen05 MMAs with TMEM accumulators, TMA-staged tiles).
+//
+// Operation ("aprender-gpu 0.32.0 -- prefill_fused.rs", module doc,
+// Algorithm 1-3): for query head h and KV head g = h / heads_per_kv, row i
+// of O is sum_{j<=i} softmax_j(scale * Q[i].K[j]) V[j], computed with an
+// online softmax.  The page does this with one warp per head on CUDA cores;
+// here the two contractions (S = Q K^T and O += P V) run on the tensor core.
+//
+// Precision: a pre-pass rounds Q, K, V (fp32, packed strides) to fp16 with
+// round-to-nearest into a workspace (10-bit mantissa, the same as TF32), the
+// softmax writes P as fp16, and every MMA accumulates in fp32.  Softmax
+// statistics (row max, row sum) and the output stay fp32.
+//
+// CTA work unit: two consecutive 128-row query tiles (A = rows q0..q0+127,
+// B = q0+128..q0+255) of one head; keys are walked in 128-row tiles up to the
+// diagonal.  Warp roles (320 threads):
+//   warps 0-3  softmax for tile A  (thread r owns TMEM lane r = query row r)
+//   warps 4-7  softmax for tile B
+//   warp  8    TMA producer: Q tiles once, then K and V tiles into a
+//              two-stage ring
+//   warp  9    TMEM allocator and MMA issuer (one thread)
+// TMEM (512 columns): per tile, S/P in 128 columns (P is written as packed
+// fp16 pairs over the first 64 columns of S) and O in head_dim columns.
+// The MMA thread ping-pongs: while softmax A works on S_A(j), the tensor core
+// runs PV_B(j-1) and S_B(j); while softmax B works, it runs PV_A(j) and
+// S_A(j+1).  tcgen05 MMAs issued by one thread execute in order, so S_t(j+1)
+// may overwrite the TMEM that held P_t(j) right after PV_t(j) is issued, and
+// the commit that signals S_t(j+1) also covers PV_t(j): once softmax t sees
+// S_t(j+1) its O accumulator is stable and can be rescaled.
+// Rescaling is conditional: the running max used for the exponentials only
+// moves when the row max grows by more than 8 (log2 units); the final O / l
+// is exact either way, and P stays below 2^8.
+// Every mbarrier wait is bounded; on a timeout a thread records
+// kStatusTimeout in the device status word, abandons its loop, and the CTA
+// still drains its copies, waits for its MMAs and frees TMEM before exiting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;            // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;            // keys per KV tile
+constexpr int kNQ = 2;              // query tiles per CTA
+constexpr int kStages = 2;          // K/V ring depth
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint64_t kDrainWaitNs = 100000000ull;  // 100 ms: copies/MMAs in flight finish in us
+
+template <int D>
+struct TcLayout {
+    static constexpr uint32_t kBoxes = D / 64;                  // 64 fp16 = 128 B per box row
+    static constexpr uint32_t kQTileBytes = kBM * D * 2;
+    static constexpr uint32_t kKTileBytes = kBN * D * 2;
+    static constexpr uint32_t kQOff = 0;
+    static constexpr uint32_t kKOff = kQOff + kNQ * kQTileBytes;
+    static constexpr uint32_t kVOff = kKOff + kStages * kKTileBytes;
+    static constexpr uint32_t kBytes = kVOff + kStages * kKTileBytes;
+    static constexpr uint32_t kSmemAlloc = kBytes + 1024;        // room to align to 1 KB
+};
+
+struct __align__(8) TcBarriers {
+    uint64_t q_full;
+    uint64_t k_full[kStages];
+    uint64_t k_empty[kStages];
+    uint64_t v_full[kStages];
+    uint64_t v_empty[kStages];
+    uint64_t s_full[kNQ];
+    uint64_t p_full[kNQ];
+    uint64_t o_final[kNQ];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t abort;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16) {
+    if (bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void record_timeout(unsigned int* status, TcBarriers* bars) {
+    atomicOr(status, kStatusTimeout);
+    atomicExch(&bars->abort, 1u);
+}
+
+// Number of KV tiles query tile `qt` attends to (0 when the tile is empty).
+__device__ __forceinline__ uint32_t kv_tiles_for(uint32_t qt, uint32_t m) {
+    return (qt * kBM < m) ? qt + 1 : 0;  // kBN == kBM: the diagonal tile index is qt
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, uint32_t m,
+                  uint32_t num_q_heads, uint32_t heads_per_kv, uint32_t q_stride,
+                  float scale_log2, unsigned int* status, uint64_t wait_ns) {
+    using L = TcLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    __shared__ TcBarriers bars;
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
+    const uint32_t pair = n_pairs - 1 - blockIdx.x / num_q_heads;  // heaviest pairs first
+    const uint32_t h = blockIdx.x % num_q_heads;
+    const uint32_t kvh = h / heads_per_kv;
+    const uint32_t qt0 = pair * kNQ;                                // first query tile index
+    uint32_t n_kv[kNQ];
+#pragma unroll
+    for (int t = 0; t < kNQ; ++t) n_kv[t] = kv_tiles_for(qt0 + t, m);
+    uint32_t n_kv_all = 0;
+#pragma unroll
+    for (int t = 0; t < kNQ; ++t) n_kv_all = max(n_kv_all, n_kv[t]);
+
+    const uint32_t sQ = smem_u32(smem + L::kQOff);
+    const uint32_t sK = smem_u32(smem + L::kKOff);
+    const uint32_t sV = smem_u32(smem + L::kVOff);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars.q_full), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&bars.k_full[s]), 1);
+            mbar_init(smem_u32(&bars.k_empty[s]), 1);
+            mbar_init(smem_u32(&bars.v_full[s]), 1);
+            mbar_init(smem_u32(&bars.v_empty[s]), 1);
+        }
+        for (int t = 0; t < kNQ; ++t) {
+            mbar_init(smem_u32(&bars.s_full[t]), 1);
+            mbar_init(smem_u32(&bars.p_full[t]), kBM);
+            mbar_init(smem_u32(&bars.o_final[t]), 1);
+        }
+        mbar_init(smem_u32(&bars.mma_done), 1);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&bars.tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(smem_u32(&bars.q_full), kNQ * L::kQTileBytes);
+            for (int t = 0; t < kNQ; ++t)
+                for (uint32_t b = 0; b < L::kBoxes; ++b)
+                    tma_load_2d(sQ + t * L::kQTileBytes + b * (kBM * 128), &tm_q,
+                                smem_u32(&bars.q_full), (int32_t)(h * D + b * 64),
+                                (int32_t)((qt0 + t) * kBM));
+            bool ok = true;
+            uint32_t issued = 0;
+            for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
+                const uint32_t st = j % kStages;
+                const uint32_t use = j / kStages;
+                if (use > 0) ok = mbar_wait(smem_u32(&bars.k_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
+                if (!ok) break;
+                mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), L::kKTileBytes);
+                for (uint32_t b = 0; b < L::kBoxes; ++b)
+                    tma_load_2d(sK + st * L::kKTileBytes + b * (kBN * 128), &tm_k,
+                                smem_u32(&bars.k_full[st]), (int32_t)(kvh * D + b * 64),
+                                (int32_t)(j * kBN));
+                if (use > 0) ok = mbar_wait(smem_u32(&bars.v_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
+                if (!ok) { issued = j + 1; break; }
+                mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), L::kKTileBytes);
+                for (uint32_t b = 0; b < L::kBoxes; ++b)
+                    tma_load_2d(sV + st * L::kKTileBytes + b * (kBN * 128), &tm_v,
+                                smem_u32(&bars.v_full[st]), (int32_t)(kvh * D + b * 64),
+                                (int32_t)(j * kBN));
+                issued = j + 1;
+            }
+            if (!ok) record_timeout(status, &bars);
+            // Drain: every copy this CTA issued must land before it exits.
+            mbar_wait(smem_u32(&bars.q_full), 0, kDrainWaitNs);
+            for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
+                const uint32_t st = j % kStages, ph = (j / kStages) & 1;
+                mbar_wait(smem_u32(&bars.k_full[st]), ph, kDrainWaitNs);
+                mbar_wait(smem_u32(&bars.v_full[st]), ph, kDrainWaitNs);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16(BF16 ? 1u : 0u, 0, 0, kBN, kBM);
+            const uint32_t idesc_pv = idesc_f16(BF16 ? 1u : 0u, 0, 1, D, kBM);
+            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, wait_ns, status, kStatusTimeout);
+            auto issue_s = [&](int t, uint32_t j) {
+                const uint32_t st = j % kStages;
+                const uint32_t qa = sQ + t * L::kQTileBytes, kb = sK + st * L::kKTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
+                    const uint32_t offk = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
+                    mma_f16_ss(tmem + t * 256, smem_desc(qa + off, 16, 1024, 2),
+                               smem_desc(kb + offk, 16, 1024, 2), idesc_s, ks > 0);
+                }
+                mma_commit(smem_u32(&bars.s_full[t]));
+            };
+            auto issue_pv = [&](int t, uint32_t j) {
+                const uint32_t st = j % kStages;
+                const uint32_t vb = sV + st * L::kKTileBytes;
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks) {
+                    // V tile is MN-major: 64-column boxes are kBN*128 bytes apart
+                    // (leading byte offset), 8-key groups 1024 bytes apart (stride).
+                    mma_f16_ts(tmem + t * 256 + 128, tmem + t * 256 + ks * 8,
+                               smem_desc(vb + ks * 2048, kBN * 128, 1024, 2), idesc_pv,
+                               (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                if (j + 1 == n_kv[t]) mma_commit(smem_u32(&bars.o_final[t]));
+            };
+            if (ok && n_kv_all > 0) {
+                ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, wait_ns, status, kStatusTimeout);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < kNQ; ++t)
+                        if (n_kv[t] > 0) issue_s(t, 0);
+                    mma_commit(smem_u32(&bars.k_empty[0]));
+                }
+            }
+            for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
+                const uint32_t st = j % kStages, ph = (j / kStages) & 1;
+                ok = mbar_wait(smem_u32(&bars.v_full[st]), ph, wait_ns, status, kStatusTimeout);
+                if (!ok) break;
+                bool k_next_ready = false;
+                const uint32_t jn = j + 1;
+                for (int t = 0; t < kNQ && ok; ++t) {
+                    if (j < n_kv[t]) {
+                        ok = mbar_wait(smem_u32(&bars.p_full[t]), j & 1, wait_ns, status, kStatusTimeout);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, j);
+                    }
+                    if (jn < n_kv[t]) {
+                        if (!k_next_ready) {
+                            ok = mbar_wait(smem_u32(&bars.k_full[jn % kStages]),
+                                           (jn / kStages) & 1, wait_ns, status, kStatusTimeout);
+                            if (!ok) break;
+                            tc_fence_after();
+                            k_next_ready = true;
+                        }
+                        issue_s(t, jn);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bars.v_empty[st]));
+                if (k_next_ready) mma_commit(smem_u32(&bars.k_empty[jn % kStages]));
+            }
+            if (!ok) record_timeout(status, &bars);
+            // Wait until every MMA this thread issued has completed.
+            mma_commit(smem_u32(&bars.mma_done));
+            mbar_wait(smem_u32(&bars.mma_done), 0, kDrainWaitNs);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int t = warp / 4;                 // query tile of this warpgroup
+        const int wq = warp % 4;                // TMEM lane quarter
+        const uint32_t row_in_tile = wq * 32 + lane;
+        const uint32_t row = (qt0 + t) * kBM + row_in_tile;
+        const uint32_t t_s = tmem + t * 256 + ((uint32_t)(wq * 32) << 16);
+        const uint32_t t_o = t_s + 128;
+        float m_used = -CUDART_INF_F;  // log2 units
+        float l_sum = 0.f;
+        bool ok = true;
+        const uint32_t nkv = n_kv[t];
+        for (uint32_t j = 0; j < nkv; ++j) {
+            ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, wait_ns, status, kStatusTimeout);
+            const bool any_fail = __any_sync(0xffffffffu, !ok);
+            if (any_fail) { ok = false; break; }
+            tc_fence_after();
+            float s[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32_sync(t_s + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+            }
+            if (j + 1 == nkv) {  // diagonal tile: keys above the row are not attended
+                const uint32_t key0 = j * kBN;
+#pragma unroll
+                for (int c = 0; c < kBN; ++c)
+                    if (key0 + c > row) s[c] = -CUDART_INF_F;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+            const float m_new = mx * scale_log2;
+            float corr = 1.f;
+            bool rescale = false;
+            if (m_new > m_used + kRescaleThreshold) {
+                corr = ex2(m_used - m_new);      // 0 on the first tile
+                rescale = (j > 0);
+                m_used = m_new;
+            }
+            const float neg_m = -m_used;
+            float rowsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], scale_log2, neg_m));
+                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], scale_log2, neg_m));
+                    rowsum += p0 + p1;
+                    pk[i] = pack_half2(p0, p1, BF16);
+                }
+                tmem_st16(t_s + c * 16, pk);
+            }
+            l_sum = fmaf(l_sum, corr, rowsum);
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float f = rescale ? corr : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32_sync(t_o + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+                    tmem_st32(t_o + c * 32, r);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.p_full[t]));
+        }
+        if (ok && nkv > 0) {
+            ok = mbar_wait(smem_u32(&bars.o_final[t]), 0, wait_ns, status, kStatusTimeout);
+            if (__any_sync(0xffffffffu, !ok)) ok = false;
+            if (ok) {
+                tc_fence_after();
+                const float inv_l = 1.0f / l_sum;
+                float* dst = o + (size_t)row * q_stride + (size_t)h * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32_sync(t_o + c * 32, r);
+                    if (row < m) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            float4 v4 = make_float4(__uint_as_float(r[i]) * inv_l,
+                                                    __uint_as_float(r[i + 1]) * inv_l,
+                                                    __uint_as_float(r[i + 2]) * inv_l,
+                                                    __uint_as_float(r[i + 3]) * inv_l);
+                            *reinterpret_cast<float4*>(dst + c * 32 + i) = v4;
+                        }
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) record_timeout(status, &bars);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// fp32 -> fp16/bf16 rounding pre-pass: q [m, q_stride] -> qh [m, hq*d] etc.
+// grid.y selects the tensor (0 = q, 1 = k, 2 = v).  Each thread converts 8
+// consecutive elements of one row (two 128-bit loads, one 128-bit store).
+template <bool BF16>
+__global__ void round_operands_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                                      const float* __restrict__ v, uint16_t* __restrict__ qh,
+                                      uint16_t* __restrict__ kh, uint16_t* __restrict__ vh,
+                                      uint32_t m, uint32_t q_cols, uint32_t kv_cols,
+                                      uint32_t q_stride, uint32_t kv_stride,
+                                      unsigned int* status) {
+    const float* src = blockIdx.y == 0 ? q : (blockIdx.y == 1 ? k : v);
+    uint16_t* dst = blockIdx.y == 0 ? qh : (blockIdx.y == 1 ? kh : vh);
+    const uint32_t cols = blockIdx.y == 0 ? q_cols : kv_cols;
+    const uint32_t stride = blockIdx.y == 0 ? q_stride : kv_stride;
+    const uint32_t per_row = cols / 8;
+    const size_t total = (size_t)m * per_row;
+    bool overflow = false;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / per_row;
+        const uint32_t c = (uint32_t)(i % per_row) * 8;
+        const float4* s4 = reinterpret_cast<const float4*>(src + r * stride + c);
+        const float4 a = __ldcs(s4), b = __ldcs(s4 + 1);
+        uint4 out;
+        out.x = pack_half2(a.x, a.y, BF16);
+        out.y = pack_half2(a.z, a.w, BF16);
+        out.z = pack_half2(b.x, b.y, BF16);
+        out.w = pack_half2(b.z, b.w, BF16);
+        if (!BF16) {
+            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+            overflow |= !(mx <= 65504.f);
+        }
+        *reinterpret_cast<uint4*>(dst + r * cols + c) = out;
+    }
+    if (__any_sync(0xffffffffu, overflow) && (threadIdx.x % 32) == 0)
+        atomicOr(status, kStatusRange);
+}
+
+__global__ void wait_timeout_selftest_kernel(unsigned int* status, uint64_t wait_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on this barrier: the bounded wait must give up.
+    if (!mbar_wait(smem_u32(&bar), 0, wait_ns, status, kStatusTimeout)) atomicOr(status, kStatusTimeout);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_operand_map(CUtensorMap* map, const void* base, uint32_t cols, uint32_t rows,
+                        uint32_t box_rows, bool bf16) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     2, const_cast<void*>(base), gdim, gstride, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+template <int D, bool BF16>
+cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, uint32_t m,
+                      uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
+                      uint32_t kv_stride, float scale, void* workspace, unsigned int* status,
+                      uint64_t wait_ns, cudaStream_t stream) {
+    using L = TcLayout<D>;
+    const uint32_t q_cols = num_q_heads * D, kv_cols = num_kv_heads * D;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* qh = reinterpret_cast<uint16_t*>(ws);
+    uint16_t* kh = reinterpret_cast<uint16_t*>(ws + align256((size_t)m * q_cols * 2));
+    uint16_t* vh = reinterpret_cast<uint16_t*>(
+        ws + align256((size_t)m * q_cols * 2) + align256((size_t)m * kv_cols * 2));
+
+    {
+        const size_t work = (size_t)m * q_cols / 8;
+        const uint32_t threads = 256;
+        uint32_t blocks = (uint32_t)std::min<size_t>((work + threads - 1) / threads, 4096);
+        round_operands_kernel<BF16><<<dim3(blocks, 3), threads, 0, stream>>>(
+            q, k, v, qh, kh, vh, m, q_cols, kv_cols, q_stride, kv_stride, status);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap tq, tk, tv;
+    if (!encode_operand_map(&tq, qh, q_cols, m, kBM, BF16) ||
+        !encode_operand_map(&tk, kh, kv_cols, m, kBN, BF16) ||
+        !encode_operand_map(&tv, vh, kv_cols, m, kBN, BF16))
+        return cudaErrorNotSupported;
+
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, BF16>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)L::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
+    prefill_tc_kernel<D, BF16><<<n_pairs * num_q_heads, kThreads, L::kSmemAlloc, stream>>>(
+        tq, tk, tv, o, m, num_q_heads, num_q_heads / num_kv_heads, q_stride, scale * kLog2e,
+        status, wait_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t prefill_tc_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                  uint32_t head_dim) {
+    const size_t qb = (size_t)m * num_q_heads * head_dim * 2;
+    const size_t kb = (size_t)m * num_kv_heads * head_dim * 2;
+    return align256(qb) + 2 * align256(kb);
+}
+
+cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, float* o,
+                              uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                              uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
+                              float scale, bool bf16, void* workspace, unsigned int* status,
+                              uint64_t wait_ns, cudaStream_t stream) {
+#define ATTN_TC_CASE(DD)                                                                     \
+    if (head_dim == DD) {                                                                    \
+        return bf16 ? launch_tc<DD, true>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, \
+                                          kv_stride, scale, workspace, status, wait_ns,       \
+                                          stream)                                            \
+                    : launch_tc<DD, false>(q, k, v, o, m, num_q_heads, num_kv_heads,          \
+                                           q_stride, kv_stride, scale, workspace, status,     \
+                                           wait_ns, stream);                                 \
+    }
+    ATTN_TC_CASE(64)
+    ATTN_TC_CASE(128)
+#undef ATTN_TC_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned int* status, uint64_t limit_ns) {
+    wait_timeout_selftest_kernel<<<1, 32>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,330 @@
+"""GPU parity: every call goes through the C ABI (libattn.so) on cuda:0 and is
+compared element by element with the fp64 CPU oracle on the same seeded
+inputs.  Tolerances: fp32 CUDA-core paths max abs <= 1e-4 and normwise
+relative <= 1e-4; tensor-core (fp16-operand) prefill max abs <= 3e-3.
+Output buffers are NaN-poisoned with canary bands on both sides."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.parity_utils import (FP32_ABS, FP32_REL, TC_ABS, compare, guarded_empty,
+                                guards_intact, heads_view, untouched_columns)
+
+pytestmark = pytest.mark.gpu
+
+FP32, FP16 = 0, 1
+
+
+@pytest.fixture(scope="module")
+def attn():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import attention_attn_prefill_causal_gb300 as a
+    assert a.attn_get_device_status() == a.ATTN_OK
+    return a
+
+
+def _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, prec, scale=0.0):
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    buf, o = guarded_empty(m * qs)
+    attn.attn_prefill_causal(dq, dk, dv, o, m, hq, hkv, d, qs, kvs, scale=scale, precision=prec)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    assert guards_intact(buf)
+    assert untouched_columns(o, m, qs, hq, d)
+    return heads_view(o, m, qs, hq, d)
+
+
+def _check_prefill(attn, m, hq, hkv, d, prec, seed, q_pad=0, kv_pad=0, mul=1.0, rows=None):
+    qs, kvs = hq * d + q_pad, hkv * d + kv_pad
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, seed, mul)
+    got = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, prec)
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs, rows=rows)
+    if rows is not None:
+        got = got[rows]
+    amax, rel = compare(got, ref)
+    if prec == FP32:
+        assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
+    else:
+        assert amax <= TC_ABS, amax
+    return amax, rel
+
+
+# ------------------------------------------------------------------ named workloads
+
+def test_workload_prefill_small_fp32(attn):
+    c = workloads.PREFILL_SMALL
+    amax, rel = _check_prefill(attn, c.m, c.num_q_heads, c.num_kv_heads, c.head_dim, FP32, c.seed)
+    print(f"{c.name}: max abs {amax:.3e} rel {rel:.3e}")
+
+
+def test_workload_prefill_2k_tensor_core(attn):
+    c = workloads.PREFILL_2K
+    amax, rel = _check_prefill(attn, c.m, c.num_q_heads, c.num_kv_heads, c.head_dim, FP16, c.seed)
+    print(f"{c.name} fp16-operand tensor path: max abs {amax:.3e} rel {rel:.3e}")
+
+
+def test_workload_prefill_2k_fp32(attn):
+    c = workloads.PREFILL_2K
+    amax, rel = _check_prefill(attn, c.m, c.num_q_heads, c.num_kv_heads, c.head_dim, FP32, c.seed)
+    print(f"{c.name} fp32 path: max abs {amax:.3e} rel {rel:.3e}")
+
+
+@pytest.mark.parametrize("prec", [FP16, FP32])
+def test_workload_prefill_16k_sampled_rows(attn, prec):
+    c = workloads.PREFILL_16K
+    rows = workloads.sample_rows(c.m, c.seed)
+    q, k, v = workloads.shape_inputs(c)
+    got = _run_prefill(attn, q, k, v, c.m, c.num_q_heads, c.num_kv_heads, c.head_dim, c.q_stride,
+                       c.kv_stride, prec)
+    assert np.isfinite(got).all()
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), c.m, c.num_q_heads,
+                                c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride, rows=rows)
+    amax, rel = compare(got[rows], ref)
+    print(f"{c.name} prec={prec}: {len(rows)} rows, max abs {amax:.3e} rel {rel:.3e}")
+    if prec == FP32:
+        assert amax <= FP32_ABS and rel <= FP32_REL
+    else:
+        assert amax <= TC_ABS
+
+
+def _run_decode(attn, q, kc, vc, hq, hkv, d, S, T, W, scale=0.0):
+    buf, out = guarded_empty(hq * d)
+    attn.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), out, hq, hkv, d, S, T, window=W, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    assert guards_intact(buf)
+    return out.view(hq, d).cpu().numpy()
+
+
+def test_workload_decode_4k(attn):
+    c = workloads.DECODE_4K
+    q, kc, vc, _, _ = workloads.shape_inputs(c)
+    got = _run_decode(attn, q, kc, vc, c.num_heads, c.kv_heads, c.head_dim, c.max_seq,
+                      c.total_seq, c.window)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), c.num_heads, c.kv_heads, c.head_dim,
+                        c.max_seq, c.total_seq, c.window)
+    amax, rel = compare(got, ref)
+    print(f"{c.name}: max abs {amax:.3e} rel {rel:.3e}")
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+def test_workload_append_then_windowed_decode_32k(attn):
+    c = workloads.DECODE_32K_WINDOW
+    q, kc, vc, kn, vn = workloads.shape_inputs(c)
+    dk, dv = kc.cuda(), vc.cuda()
+    pos = c.total_seq - 1
+    attn.kv_append(kn.cuda(), vn.cuda(), dk, dv, c.kv_heads, c.head_dim, c.max_seq, pos)
+    buf, out = guarded_empty(c.num_heads * c.head_dim)
+    attn.attn_decode(q.cuda(), dk, dv, out, c.num_heads, c.kv_heads, c.head_dim, c.max_seq,
+                     c.total_seq, window=c.window)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    assert guards_intact(buf)
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    oracle.kv_append(kn.numpy(), vn.numpy(), kh, vh, c.kv_heads, c.head_dim, c.max_seq, pos)
+    np.testing.assert_array_equal(dk[:, pos].cpu().numpy(), kh[:, pos])
+    np.testing.assert_array_equal(dv[:, pos].cpu().numpy(), vh[:, pos])
+    ref = oracle.decode(q.numpy(), kh, vh, c.num_heads, c.kv_heads, c.head_dim, c.max_seq,
+                        c.total_seq, c.window)
+    amax, rel = compare(out.view(c.num_heads, c.head_dim).cpu().numpy(), ref)
+    print(f"{c.name}: max abs {amax:.3e} rel {rel:.3e}")
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+# ------------------------------------------------------------------ prefill edge cases
+
+@pytest.mark.parametrize("m", [1, 2, 31, 127, 128, 129, 255, 256, 257, 300, 511, 640])
+@pytest.mark.parametrize("prec", [FP16, FP32])
+def test_prefill_ragged_lengths(attn, m, prec):
+    _check_prefill(attn, m, 4, 2, 128, prec, seed=100 + m)
+
+
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (3, 3), (7, 1), (8, 2), (14, 2)])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("prec", [FP16, FP32])
+def test_prefill_head_configs(attn, hq, hkv, d, prec):
+    _check_prefill(attn, 300, hq, hkv, d, prec, seed=hq * 10 + hkv + d)
+
+
+@pytest.mark.parametrize("d", [32, 64])
+def test_prefill_fp32_small_head_dims(attn, d):
+    _check_prefill(attn, 200, 6, 2, d, FP32, seed=d)
+
+
+@pytest.mark.parametrize("prec", [FP16, FP32])
+def test_prefill_padded_strides(attn, prec):
+    _check_prefill(attn, 333, 6, 2, 128, prec, seed=7, q_pad=64, kv_pad=128)
+
+
+@pytest.mark.parametrize("prec", [FP16, FP32])
+def test_prefill_single_packed_buffer(attn, prec):
+    """Q, K, V as column slices of one [M, (Hq+2Hkv)D] projection output with
+    equal strides (the page's zero-copy packed layout)."""
+    m, hq, hkv, d = 260, 4, 2, 128
+    W = (hq + 2 * hkv) * d
+    g = torch.Generator().manual_seed(55)
+    buf = torch.randn(m, W, generator=g)
+    dbuf = buf.cuda()
+    flat = dbuf.view(-1)
+    obuf, o = guarded_empty(m * W)
+    attn.attn_prefill_causal(flat, flat[hq * d:], flat[(hq + hkv) * d:], o, m, hq, hkv, d, W, W,
+                             precision=prec)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK and guards_intact(obuf)
+    got = heads_view(o, m, W, hq, d)
+    nb = buf.numpy().reshape(-1)
+    ref = oracle.prefill_causal(nb, nb[hq * d:], nb[(hq + hkv) * d:], m, hq, hkv, d, W, W)
+    amax, rel = compare(got, ref)
+    assert amax <= (FP32_ABS if prec == FP32 else TC_ABS)
+
+
+@pytest.mark.parametrize("prec", [FP16, FP32])
+def test_prefill_explicit_scale(attn, prec):
+    m, hq, hkv, d = 150, 2, 1, 64
+    qs, kvs = hq * d, hkv * d
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, 9)
+    got = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, prec, scale=0.05)
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs, scale=0.05)
+    amax, _ = compare(got, ref)
+    assert amax <= (FP32_ABS if prec == FP32 else TC_ABS)
+
+
+def test_prefill_rows_beyond_m_untouched(attn):
+    """A buffer with extra rows past m keeps them poisoned (no write past m)."""
+    m, hq, hkv, d = 130, 2, 2, 128
+    qs = hq * d
+    q, k, v = workloads.prefill_inputs(m, qs, hkv * d, 3)
+    for prec in (FP16, FP32):
+        buf, o = guarded_empty((m + 126) * qs)
+        attn.attn_prefill_causal(q.cuda(), k.cuda(), v.cuda(), o, m, hq, hkv, d, qs, hkv * d,
+                                 precision=prec)
+        torch.cuda.synchronize()
+        assert torch.isnan(o[m * qs:]).all().item()
+        assert torch.isfinite(o[: m * qs]).all().item()
+
+
+def test_prefill_tensor_path_rejects_fp16_overflow(attn):
+    """An input beyond the fp16 range is flagged (ATTN_ERR_RANGE) by the
+    rounding pre-pass instead of silently producing inf."""
+    m, hq, hkv, d = 64, 1, 1, 64
+    q, k, v = workloads.prefill_inputs(m, d, d, 4)
+    k[5, 3] = 1.0e5
+    buf, o = guarded_empty(m * d)
+    attn.attn_prefill_causal(q.cuda(), k.cuda(), v.cuda(), o, m, hq, hkv, d, d, d, precision=FP16)
+    assert attn.attn_get_device_status() == attn.ATTN_ERR_RANGE
+    assert attn.attn_get_device_status() == attn.ATTN_OK  # cleared by the read
+
+
+# ------------------------------------------------------------------ decode edge cases
+
+@pytest.mark.parametrize("T", [1, 2, 31, 32, 33, 100, 1023, 4095, 4096])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_decode_lengths(attn, T, d):
+    hq, hkv, S = 8, 2, 4096
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=T + d)
+    got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, T, 0)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, 0)
+    amax, rel = compare(got, ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 4), (8, 1), (12, 1), (16, 2), (24, 2), (32, 8)])
+def test_decode_gqa_groups(attn, hq, hkv):
+    """Groups above 8 query heads per KV head take several CTA head-groups."""
+    d, S, T = 128, 2000, 1777
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=hq * 7 + hkv)
+    got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, T, 0)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, 0)
+    amax, rel = compare(got, ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+@pytest.mark.parametrize("T,W", [(4096, 1), (4096, 7), (4096, 4095), (4096, 4096), (4096, 5000),
+                                 (3000, 1024), (33, 32), (2, 1)])
+def test_decode_windows(attn, T, W):
+    hq, hkv, d, S = 8, 2, 128, 4096
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=T * 3 + W)
+    got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, T, W)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, W)
+    amax, rel = compare(got, ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+def test_decode_masked_positions_keep_their_minus_1e4_weight(attn):
+    """When every live score lies below -1e4 the masked positions (score
+    replaced by -1e4) dominate the softmax; the combine then reads the masked
+    V rows and reproduces the page's replaced-score result.  Scores of
+    magnitude ~1e4 carry an fp32 resolution of ~1e-3 (log2 units), so the
+    bound here is 1e-2 rather than the 1e-4 of ordinary inputs."""
+    hq, hkv, d, S, T, W = 2, 1, 64, 256, 200, 50
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=77)
+    q[:] = 0.0
+    q[:, 0] = 1.0
+    kc[0, :, 0] = -1.0e4 - 1.0 + torch.linspace(-0.5, 0.5, S)
+    got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, T, W, scale=1.0)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, W, scale=1.0)
+    amax, _ = compare(got, ref)
+    assert amax <= 1e-2, amax
+    # the masked rows really carry weight here
+    ref_live = oracle.decode(q.numpy(), np.ascontiguousarray(kc.numpy()[:, T - W:T]),
+                             np.ascontiguousarray(vc.numpy()[:, T - W:T]), hq, hkv, d, W, W,
+                             scale=1.0)
+    assert np.abs(ref - ref_live).max() > 0.1
+
+
+def test_decode_scale_argument(attn):
+    hq, hkv, d, S, T = 4, 2, 64, 512, 300
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=5)
+    got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, T, 0, scale=0.3)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, 0, scale=0.3)
+    amax, rel = compare(got, ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+def test_prefill_rows_match_decode_on_gpu(attn):
+    """Cross-form on the GPU: prefill row i equals decode over i+1 cache rows."""
+    m, hq, hkv, d = 96, 4, 2, 128
+    q, k, v = workloads.prefill_inputs(m, hq * d, hkv * d, 31)
+    pre = _run_prefill(attn, q, k, v, m, hq, hkv, d, hq * d, hkv * d, FP32)
+    kc = k.view(m, hkv, d).transpose(0, 1).contiguous()
+    vc = v.view(m, hkv, d).transpose(0, 1).contiguous()
+    for i in (0, 1, 47, 95):
+        qi = q[i, : hq * d].view(hq, d).contiguous()
+        dec = _run_decode(attn, qi, kc, vc, hq, hkv, d, m, i + 1, 0)
+        assert np.abs(dec - pre[i]).max() <= 2 * FP32_ABS
+
+
+# ------------------------------------------------------------------ kv_append
+
+def test_kv_append_bit_exact(attn):
+    hkv, d, S = 4, 128, 64
+    g = torch.Generator().manual_seed(3)
+    kc, vc = torch.randn(hkv, S, d, generator=g), torch.randn(hkv, S, d, generator=g)
+    ks, vs = torch.randn(hkv, d, generator=g), torch.randn(hkv, d, generator=g)
+    for pos in (0, 17, S - 1):
+        dk, dv = kc.cuda(), vc.cuda()
+        attn.kv_append(ks.cuda(), vs.cuda(), dk, dv, hkv, d, S, pos)
+        kh, vh = kc.numpy().copy(), vc.numpy().copy()
+        oracle.kv_append(ks.numpy(), vs.numpy(), kh, vh, hkv, d, S, pos)
+        np.testing.assert_array_equal(dk.cpu().numpy(), kh)
+        np.testing.assert_array_equal(dv.cpu().numpy(), vh)
+    dk = kc.cuda()
+    attn.kv_append(ks.cuda(), None, dk, None, hkv, d, S, 9)
+    kh = kc.numpy().copy()
+    oracle.kv_append(ks.numpy(), None, kh, None, hkv, d, S, 9)
+    np.testing.assert_array_equal(dk.cpu().numpy(), kh)
+
+
+# ------------------------------------------------------------------ failure detection
+
+def test_bounded_wait_times_out_and_context_survives(attn):
+    """A wait on an mbarrier nothing completes gives up after ~1 ms and the
+    kernel returns; the status word reports the timeout and the context keeps
+    working."""
+    assert attn.attn_selftest_wait_timeout(1000) == attn.ATTN_ERR_TIMEOUT
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    _check_prefill(attn, 200, 2, 1, 128, FP16, seed=1)
