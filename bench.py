@@ -1,0 +1,605 @@
+"""Benchmark of the attention hot path on GB300: one JSON line on rank 0.
+
+Headline workload (the decode configuration): 12 query heads over 2 KV heads,
+head_dim 128, a 4096-row cache, no window.  One step = kv_append of the new
+K/V row at position total_seq-1 followed by attn_decode over all 4096 rows.
+Metric value = algorithmic K+V bytes (2 * kv_heads * total_seq * head_dim * 4)
+per step x steps / device time, in GB/s.  The caches rotate over enough
+replicas that every step reads them cold from HBM (the replicas together
+exceed twice the 129 MB L2).  Steps run as CUDA-graph replays so that host
+launch overhead does not bound a 5-microsecond step.
+
+The same line carries the causal-prefill half of the metric (TFLOP/s of the
+tensor-core path on the 2048- and 16384-token prefill workloads), the
+roofline of the dominant kernel of each, an end-to-end number through the
+Python API with host buffers, the fp64 CPU oracle timed on the host cores,
+and the SM clocks sampled during the timed region.
+
+--impl reference times the oracle (the plain CPU definition) on the host
+cores instead, on the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "decode KV GB/s and causal prefill TFLOP/s vs GB300 roofline (1 GPU)"
+L2_BYTES = 129 * 1024 * 1024
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "attention_attn_prefill_causal_gb300", "csrc")
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def aggregate(per_rank_seconds: float, per_rank_units: float, ws: int):
+    """Whole-job throughput: units of all ranks / max seconds over ranks."""
+    if ws > 1:
+        t = torch.tensor([per_rank_seconds], dtype=torch.float64)
+        u = torch.tensor([per_rank_units], dtype=torch.float64)
+        if torch.distributed.get_backend() == "nccl":
+            t, u = t.cuda(), u.cuda()
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+        return float(t.item()), float(u.item())
+    return per_rank_seconds, per_rank_units
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, files):
+    """DRAM bytes per launch from a committed ncu capture, only while the
+    kernel's sources are unchanged since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not t or t.get("source_sha") != source_sha(files):
+        return None
+    return t.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) in a background process; keeps the
+    samples whose timestamps fall inside [t0, t1] (host clock)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def pump():
+            for line in self.proc.stdout:
+                self.lines.append((time.time(), line.strip()))
+        self.thread = threading.Thread(target=pump, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return None
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if t0 - 0.25 <= ts <= t1 + 0.25]
+        if not inside and rows:  # timed region shorter than one sample period
+            mid = 0.5 * (t0 + t1)
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))[1]]
+        if not inside:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in inside if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for n, v in zip(names, r[6:10]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": num(inside[0][3]),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def make_graph(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # make sure lazily created state exists before capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+# ---------------------------------------------------------------- decode (headline)
+
+class DecodeBench:
+    def __init__(self, attn, shape, device):
+        self.attn, self.c, self.dev = attn, shape, device
+        q, kc, vc, kn, vn = workloads.decode_inputs(shape.num_heads, shape.kv_heads,
+                                                    shape.head_dim, shape.max_seq, shape.seed,
+                                                    append=True)
+        self.host = (q, kc, vc, kn, vn)
+        cache_bytes = 2 * kc.numel() * 4
+        self.R = max(2, math.ceil(2 * L2_BYTES / cache_bytes))
+        self.kc = [kc.to(device) for _ in range(self.R)]
+        self.vc = [vc.to(device) for _ in range(self.R)]
+        self.q, self.kn, self.vn = q.to(device), kn.to(device), vn.to(device)
+        self.out = torch.empty(shape.num_heads, shape.head_dim, device=device)
+        ws = attn.attn_decode_workspace_size(shape.num_heads, shape.kv_heads, shape.head_dim,
+                                             shape.total_seq, shape.window)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.pos = shape.total_seq - 1
+        self.launches_per_step = 3  # kv_append, split, combine
+
+    def step(self, i, stream, append=True):
+        c, a = self.c, self.attn
+        r = i % self.R
+        if append:
+            a.kv_append(self.kn, self.vn, self.kc[r], self.vc[r], c.kv_heads, c.head_dim,
+                        c.max_seq, self.pos, stream=stream)
+        a.attn_decode(self.q, self.kc[r], self.vc[r], self.out, c.num_heads, c.kv_heads,
+                      c.head_dim, c.max_seq, c.total_seq, window=c.window, workspace=self.ws,
+                      stream=stream)
+
+    def graphs(self, stream, append=True):
+        def chunk():
+            for i in range(self.R):
+                self.step(i, stream, append)
+        return make_graph(chunk, stream)
+
+    def check(self):
+        """Untimed parity check of what the bench times (replica 0)."""
+        import oracle
+        c = self.c
+        q, kc, vc, kn, vn = self.host
+        kh, vh = kc.numpy().copy(), vc.numpy().copy()
+        oracle.kv_append(kn.numpy(), vn.numpy(), kh, vh, c.kv_heads, c.head_dim, c.max_seq,
+                         self.pos)
+        ref = oracle.decode(q.numpy(), kh, vh, c.num_heads, c.kv_heads, c.head_dim, c.max_seq,
+                            c.total_seq, c.window)
+        s = torch.cuda.current_stream()
+        self.step(0, s)
+        torch.cuda.synchronize()
+        return float(np.abs(self.out.cpu().numpy() - ref).max())
+
+
+def run_graph_steps(graph, steps_per_graph, rem_graph, steps):
+    """Replay graphs to execute exactly `steps` steps."""
+    full, rem = divmod(steps, steps_per_graph)
+    for _ in range(full):
+        graph.replay()
+    if rem:
+        rem_graph[rem].replay()
+
+
+def time_steps(graph, R, rem_graphs, steps, stream):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        run_graph_steps(graph, R, rem_graphs, steps)
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+class RemainderGraphs(dict):
+    """Graphs of n < R steps, captured on first use."""
+
+    def __init__(self, bench, stream, append=True):
+        super().__init__()
+        self.bench, self.stream, self.append = bench, stream, append
+
+    def __missing__(self, n):
+        def f():
+            for i in range(n):
+                self.bench.step(i, self.stream, self.append)
+        g = make_graph(f, self.stream)
+        self[n] = g
+        return g
+
+
+def remainder_graphs(bench, stream, append=True):
+    return RemainderGraphs(bench, stream, append)
+
+
+# ---------------------------------------------------------------- prefill (companion)
+
+class PrefillBench:
+    def __init__(self, attn, shape, device):
+        self.attn, self.c, self.dev = attn, shape, device
+        q, k, v = workloads.shape_inputs(shape)
+        self.host = (q, k, v)
+        in_bytes = (q.numel() + k.numel() + v.numel() + q.numel()) * 4
+        self.R = 1 if in_bytes > 2 * L2_BYTES else max(2, math.ceil(2 * L2_BYTES / in_bytes))
+        self.q = [q.to(device) for _ in range(self.R)]
+        self.k = [k.to(device) for _ in range(self.R)]
+        self.v = [v.to(device) for _ in range(self.R)]
+        self.o = [torch.empty_like(self.q[0]) for _ in range(self.R)]
+        ws = attn.attn_prefill_workspace_size(shape.m, shape.num_q_heads, shape.num_kv_heads,
+                                              shape.head_dim, attn.ATTN_PREC_FP16)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+
+    def call(self, i, stream):
+        c, a, r = self.c, self.attn, i % self.R
+        a.attn_prefill_causal(self.q[r], self.k[r], self.v[r], self.o[r], c.m, c.num_q_heads,
+                              c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride,
+                              precision=a.ATTN_PREC_FP16, workspace=self.ws, stream=stream)
+
+    def check(self):
+        import oracle
+        c = self.c
+        q, k, v = self.host
+        rows = workloads.sample_rows(c.m, c.seed, 16, 16, 32)
+        ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), c.m, c.num_q_heads,
+                                    c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride, rows=rows)
+        self.call(0, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        got = self.o[0].view(c.m, c.q_stride)[:, : c.num_q_heads * c.head_dim]
+        got = got.cpu().numpy().reshape(c.m, c.num_q_heads, c.head_dim)[rows]
+        return float(np.abs(got - ref).max())
+
+
+def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
+    pb = PrefillBench(attn, shape, device)
+    err = pb.check()
+
+    def chunk():
+        for i in range(pb.R):
+            pb.call(i, stream)
+    g = make_graph(chunk, stream)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, math.ceil(calls / pb.R))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+    end.synchronize()
+    secs = start.elapsed_time(end) / 1e3
+    n = reps * pb.R
+    per_call = secs / n
+    flops = shape.flops()
+    tflops = flops / per_call / 1e12
+    peak_key = "bf16_tflops_sustained" if secs > 1.0 else "bf16_tflops"
+    peak = float(peaks[peak_key])
+    traffic = traffic_for("prefill_tc_kernel", ["prefill_tc.cu", "sm103_ptx.cuh"])
+
+    # end to end through the Python API with host buffers (pinned)
+    q, k, v = pb.host
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    ho = torch.empty_like(hq).pin_memory()
+    e_calls = 3
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    c = shape
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(e_calls):
+            pb.q[0].copy_(hq, non_blocking=True)
+            pb.k[0].copy_(hk, non_blocking=True)
+            pb.v[0].copy_(hv, non_blocking=True)
+            attn.attn_prefill_causal(pb.q[0], pb.k[0], pb.v[0], pb.o[0], c.m, c.num_q_heads,
+                                     c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride,
+                                     precision=attn.ATTN_PREC_FP16, workspace=pb.ws, stream=stream)
+            ho.copy_(pb.o[0], non_blocking=True)
+        t1.record(stream)
+    t1.synchronize()
+    e2e_per_call = t0.elapsed_time(t1) / 1e3 / e_calls
+    h2d = (q.numel() + k.numel() + v.numel()) * 4
+    d2h = q.numel() * 4
+    return {
+        "workload": shape.name,
+        "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(per_call * 1e3, 4),
+        "calls": n, "flops_per_call": flops,
+        "dtype": "fp16 operands (round-to-nearest from fp32), fp32 accumulate and output",
+        "l2": (f"inputs {pb.R} rotating replicas" if pb.R > 1 else "inputs larger than 2x L2"),
+        "max_abs_err_sampled_rows": err,
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_key} ({peak_src}; fp16 dense peak = bf16 nominal)",
+                     "kernel": "attn_prefill_causal call (rounding pre-pass + prefill_tc_kernel)"},
+        "e2e": {"value": round(flops / e2e_per_call / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches_per_call": 2,
+    }
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def cpu_baseline_decode(shape, budget_s=10.0, max_steps=2000):
+    import oracle
+    q, kc, vc, kn, vn = workloads.decode_inputs(shape.num_heads, shape.kv_heads, shape.head_dim,
+                                                shape.max_seq, shape.seed, append=True)
+    q, kh, vh, kn, vn = q.numpy(), kc.numpy().copy(), vc.numpy().copy(), kn.numpy(), vn.numpy()
+    cores = oracle.max_threads()
+    pos = shape.total_seq - 1
+    steps, t0 = 0, time.perf_counter()
+    while steps < max_steps and time.perf_counter() - t0 < budget_s:
+        oracle.kv_append(kn, vn, kh, vh, shape.kv_heads, shape.head_dim, shape.max_seq, pos)
+        oracle.decode(q, kh, vh, shape.num_heads, shape.kv_heads, shape.head_dim, shape.max_seq,
+                      shape.total_seq, shape.window)
+        steps += 1
+    secs = time.perf_counter() - t0
+    return steps, secs, cores
+
+
+# ---------------------------------------------------------------- arms
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    shape = workloads.DECODE_4K
+    import oracle
+    q, kc, vc, kn, vn = workloads.decode_inputs(shape.num_heads, shape.kv_heads, shape.head_dim,
+                                                shape.max_seq, shape.seed, append=True)
+    q, kh, vh, kn, vn = q.numpy(), kc.numpy().copy(), vc.numpy().copy(), kn.numpy(), vn.numpy()
+    pos = shape.total_seq - 1
+
+    def step():
+        oracle.kv_append(kn, vn, kh, vh, shape.kv_heads, shape.head_dim, shape.max_seq, pos)
+        oracle.decode(q, kh, vh, shape.num_heads, shape.kv_heads, shape.head_dim, shape.max_seq,
+                      shape.total_seq, shape.window)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    bytes_step = shape.kv_bytes_algorithmic()
+    value = bytes_step * args.steps / secs / 1e9
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": shape.name, "num_heads": shape.num_heads,
+                   "kv_heads": shape.kv_heads, "head_dim": shape.head_dim,
+                   "total_seq": shape.total_seq, "window": shape.window,
+                   "step": "kv_append + decode, fp64 CPU oracle"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{args.steps} full decode steps (all 12 heads, 4096 rows)"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def our_arm(args):
+    ws, rank, local = dist_env()
+    init_dist(ws, "nccl")
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import attention_attn_prefill_causal_gb300 as attn
+
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device=device)
+    shape = workloads.DECODE_4K
+    db = DecodeBench(attn, shape, device)
+    err = db.check()
+    if err > 1e-4:
+        raise SystemExit(f"decode parity check failed before timing: max abs error {err}")
+
+    g = db.graphs(stream)
+    rem = remainder_graphs(db, stream)
+    time_steps(g, db.R, rem, args.warmup, stream)  # warm-up: W untimed steps
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    secs = time_steps(g, db.R, rem, args.steps, stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    barrier(ws)
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+
+    bytes_step = shape.kv_bytes_algorithmic()
+    max_secs, total_bytes = aggregate(secs, bytes_step * args.steps, ws)
+    value = total_bytes / max_secs / 1e9
+
+    # Dominant kernel (the decode call: split + combine) timed alone in the
+    # same way: graphs of decode calls over the rotating replicas.
+    gd = db.graphs(stream, append=False)
+    remd = remainder_graphs(db, stream, append=False)
+    time_steps(gd, db.R, remd, db.R * 4, stream)
+    n_dec = max(args.steps, db.R * 8)
+    dsecs = time_steps(gd, db.R, remd, n_dec, stream)
+    per_decode = dsecs / n_dec
+    achieved = bytes_step / per_decode / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    traffic = traffic_for("attn_decode", ["decode.cu"])
+
+    # End to end through the Python API: per step, H2D of q, k_new, v_new from
+    # pinned host memory, kv_append + attn_decode, D2H of the output.
+    q, kc, vc, kn, vn = db.host
+    hq, hkn, hvn = q.pin_memory(), kn.pin_memory(), vn.pin_memory()
+    hout = torch.empty(shape.num_heads, shape.head_dim).pin_memory()
+    e_steps = min(args.steps, 2000)
+    for i in range(3):
+        db.step(i, stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(e_steps):
+            db.q.copy_(hq, non_blocking=True)
+            db.kn.copy_(hkn, non_blocking=True)
+            db.vn.copy_(hvn, non_blocking=True)
+            db.step(i, stream)
+            hout.copy_(db.out, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e_secs = e0.elapsed_time(e1) / 1e3
+    e_max, e_bytes = aggregate(e_secs, bytes_step * e_steps, ws)
+
+    prefill = []
+    if not args.no_prefill:
+        for ps in (workloads.PREFILL_2K, workloads.PREFILL_16K):
+            calls = 200 if ps.m <= 4096 else 20
+            prefill.append(bench_prefill(attn, ps, device, stream, calls, peaks, peak_src))
+
+    status = attn.attn_get_device_status()
+    if status != attn.ATTN_OK:
+        raise SystemExit(f"device status after the run: {attn.attn_status_string(status)}")
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        steps_c, secs_c, cores = cpu_baseline_decode(shape)
+        cpu = {"value": round(bytes_step * steps_c / secs_c / 1e9, 3), "unit": "GB/s",
+               "cores": cores, "kind": "oracle",
+               "sample": f"{steps_c} full decode steps (kv_append + decode, all heads) "
+                         f"in {secs_c:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(max_secs / args.steps * 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": shape.name, "num_heads": shape.num_heads,
+                       "kv_heads": shape.kv_heads, "head_dim": shape.head_dim,
+                       "max_seq": shape.max_seq, "total_seq": shape.total_seq,
+                       "window": shape.window,
+                       "step": "kv_append at total_seq-1 + attn_decode (CUDA-graph replays)",
+                       "l2": f"inputs larger than L2: {db.R} rotating cache replicas "
+                             f"({db.R * 2 * shape.kv_heads * shape.max_seq * shape.head_dim * 4 // 2**20} MiB)",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "bytes_per_step": bytes_step},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
+                         "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+                         "peak_source": f"hbm_gbs ({peak_src})",
+                         "kernel": "attn_decode call (decode_split_kernel + decode_combine_kernel)",
+                         "ms_per_launch": round(per_decode * 1e3, 5)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e_bytes / e_max / 1e9, 3), "unit": "GB/s",
+                    "h2d_bytes_per_step": (q.numel() + kn.numel() + vn.numel()) * 4,
+                    "d2h_bytes_per_step": shape.num_heads * shape.head_dim * 4,
+                    "note": "K/V caches stay resident in HBM (decode state); per-step inputs "
+                            "and the output cross the host link"},
+            "gpu_launches": args.steps * db.launches_per_step,
+            "clocks": clocks,
+            "parity_max_abs_err": err,
+            "prefill": prefill,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(ws)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+    return our_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,71 @@
+"""Host-side logic of bench.py (no GPU): multi-rank aggregation over gloo,
+clock-sample parsing, and the reference (oracle) arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    secs, units = bench.aggregate(1.0 + rank, 10.0 * (rank + 1), world)
+    bench.barrier(world)
+    q.put((rank, secs, units))
+    torch.distributed.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    """Whole-job value = units summed over ranks / max time over ranks."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, secs, units in res:
+        assert secs == 2.0 and units == 30.0
+
+
+def test_clock_summary_parsing():
+    s = bench.ClockSampler(0)
+    s.proc = object()
+    now = 1000.0
+    s.lines = [(now + 0.1, "2026/12/02 10:00:00.000, 0, 1965, 2070, 900.1, 0x0, Not Active, "
+                           "Not Active, Not Active, Active"),
+               (now + 0.3, "2026/12/02 10:00:00.200, 0, 1980, 2070, 950.0, 0x0, Not Active, "
+                           "Not Active, Not Active, Not Active"),
+               (now + 9.0, "2026/12/02 10:00:09.000, 0, 500, 2070, 50.0, 0x0, Not Active, "
+                           "Not Active, Not Active, Not Active")]
+    out = s.summary(now, now + 0.4)
+    assert out["sm_mhz"] == pytest.approx(1972.5)
+    assert out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["samples"] == 2
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["metric"] == bench.METRIC
