@@ -19,7 +19,7 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "ATTN_ERR_RANGE", "ATTN_PREC_FP32", "ATTN_PREC_FP16", "ATTN_PREC_BF16",
     "AttnError", "lib", "library_path", "attn_prefill_causal", "attn_prefill_workspace_size",
-    "attn_decode", "attn_decode_workspace_size", "kv_append", "attn_status_string",
+    "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc", "kv_append", "attn_status_string",
     "attn_last_error_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "exported_symbols",
 ]
@@ -47,6 +47,8 @@ _SIGS = {
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _f32, _vp, _sz,
                          _vp]),
     "attn_decode_workspace_size": (_sz, [_u32, _u32, _u32, _u32, _u32]),
+    "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _f32,
+                                 _vp]),
     "kv_append": (_i, [_vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _vp]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_last_error_string": (ctypes.c_char_p, []),
@@ -140,6 +142,16 @@ def attn_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq
                          head_dim, max_seq, total_seq, window, float(scale), _ptr(workspace),
                          workspace_bytes, _stream(stream))
     return _check(st, "attn_decode", check)
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq,
+                        total_seq, window=0, scale=0.0, stream=None, check=True):
+    """attn_decode with the library's fixed scratch instead of a workspace
+    (C: attn_decode_noalloc).  For callers that cannot allocate."""
+    st = lib.attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads,
+                                 kv_heads, head_dim, max_seq, total_seq, window, float(scale),
+                                 _stream(stream))
+    return _check(st, "attn_decode_noalloc", check)
 
 
 def kv_append(k_src, v_src, k_cache, v_cache, kv_heads, head_dim, max_seq, position, stream=None,

@@ -69,6 +69,10 @@ attn_status_t record_cuda_error(cudaError_t err) {
     return ATTN_ERR_CUDA;
 }
 
+void set_last_error(const char* msg) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "%s", msg);
+}
+
 }  // namespace attn
 
 using namespace attn;

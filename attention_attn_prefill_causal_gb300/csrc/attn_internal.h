@@ -24,6 +24,9 @@ int device_sm_count();
 // Record a CUDA error for attn_last_error_string() and map it to a status.
 attn_status_t record_cuda_error(cudaError_t err);
 
+// Set the text attn_last_error_string() returns on this host thread.
+void set_last_error(const char* msg);
+
 // ---------------------------------------------------------------- decode
 struct DecodePlan {
     uint32_t window_start;

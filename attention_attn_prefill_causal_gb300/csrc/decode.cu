@@ -29,6 +29,8 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
+#include <mutex>
 
 #include "attn_internal.h"
 
@@ -352,3 +354,69 @@ cudaError_t launch_kv_append(const float* k_src, const float* v_src, float* k_ca
 }
 
 }  // namespace attn
+
+// ---------------------------------------------------------------------------
+// attn_decode_noalloc: decode with a fixed, library-owned scratch buffer.
+//
+// Some callers cannot hand this library a workspace and must not see it call
+// cudaMalloc: an engine that has already carved all of device memory into
+// its own pools (a KV-cache pool that owns every free byte), a plugin
+// interface that passes only input and output pointers, or a latency-bound
+// loop that forbids allocation and the implicit synchronisation it can bring.
+// For them the split partials live in one file-scope device array of
+// kNoAllocScratchBytes.  Every GPU that loads this library keeps that array
+// resident until the process exits.  The array is shared by every call on a
+// device and keeps the last call's contents; the decode kernels overwrite
+// every partial they later read, so nothing in it has to start at zero.  Two
+// calls that overlap on the GPU (different streams, or graphs replayed
+// concurrently) race on the array and corrupt each other's results.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[kNoAllocScratchBytes];
+}  // namespace
+
+namespace attn {
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static cudaError_t noalloc_scratch_address(void** out) {
+    static void* addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+}  // namespace attn
+
+extern "C" attn_status_t attn_decode_noalloc(const float* q, const float* k_cache,
+                                             const float* v_cache, float* out,
+                                             uint32_t num_heads, uint32_t kv_heads,
+                                             uint32_t head_dim, uint32_t max_seq,
+                                             uint32_t total_seq, uint32_t window, float scale,
+                                             void* stream) {
+    const size_t need = attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window);
+    if (need > kNoAllocScratchBytes) {
+        char msg[160];
+        std::snprintf(msg, sizeof(msg),
+                      "attn_decode_noalloc: these sizes need %zu bytes of scratch, more than the "
+                      "fixed %zu-byte buffer",
+                      need, kNoAllocScratchBytes);
+        attn::set_last_error(msg);
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    void* scratch = nullptr;
+    const cudaError_t e = attn::noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return attn::record_cuda_error(e);
+    return attn_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq,
+                       total_seq, window, scale, scratch, kNoAllocScratchBytes, stream);
+}

@@ -131,6 +131,28 @@ size_t attn_decode_workspace_size(uint32_t num_heads, uint32_t kv_heads, uint32_
                                   uint32_t total_seq, uint32_t window);
 
 /*
+ * attn_decode_noalloc -- attn_decode without a caller workspace.  The pages
+ * have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory or pass a workspace (an engine that owns every free
+ * byte of HBM in its own pools, a plugin interface that hands over only
+ * input and output pointers, a loop where allocation is not allowed).
+ *
+ * Same arguments, results and validation as attn_decode, minus the
+ * workspace.  The split partials live in a fixed 4 MiB device array inside
+ * libattn (resident on every GPU that loads the library, until exit); sizes
+ * whose attn_decode_workspace_size() exceeds 4 MiB are rejected with
+ * ATTN_ERR_UNSUPPORTED and a message in attn_last_error_string().  The call
+ * allocates nothing.  Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls on a device share the array:
+ * calls that overlap on the GPU race and corrupt each other's output.
+ */
+attn_status_t attn_decode_noalloc(const float* q, const float* k_cache, const float* v_cache,
+                                  float* out, uint32_t num_heads, uint32_t kv_heads,
+                                  uint32_t head_dim, uint32_t max_seq, uint32_t total_seq,
+                                  uint32_t window, float scale, void* stream);
+
+/*
  * kv_append -- write one new K row and one new V row into the caches.
  *
  * Defined by "soft3/glia/run/backend/honeycrisp/kernels/attention.rs",
