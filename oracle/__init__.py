@@ -69,6 +69,11 @@ def _load():
             lib.oracle_kv_append.argtypes = [
                 _f32p, _f32p, _f32p, _f32p, ctypes.c_uint32, ctypes.c_uint32,
                 ctypes.c_uint32, ctypes.c_uint32]
+            lib.oracle_decode_append.restype = ctypes.c_int
+            lib.oracle_decode_append.argtypes = [
+                _f32p, _f32p, _f32p, _f32p, _f32p, _f32p, _f32p, ctypes.c_uint32,
+                ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                ctypes.c_uint32, ctypes.c_uint32, ctypes.c_double, _f64p, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -165,3 +170,28 @@ def kv_append(k_src, v_src, k_cache, v_cache, kv_heads, head_dim, max_seq, posit
         kv_heads, head_dim, max_seq, position)
     if rc != 0:
         raise ValueError("oracle_kv_append rejected its arguments")
+
+
+def decode_append(q, k_new, v_new, k_cache, v_cache, num_heads, kv_heads, head_dim, max_seq,
+                  total_seq, position, window=0, scale=None, rope_cos=None, rope_sin=None,
+                  nthreads=0):
+    """Fused (RoPE +) append + decode in fp64; updates the fp32 numpy caches
+    in place and returns out [num_heads, head_dim] float64."""
+    lib = _load()
+    q, kn, vn = _as_f32(q), _as_f32(k_new), _as_f32(v_new)
+    for c in (k_cache, v_cache):
+        if not (isinstance(c, np.ndarray) and c.flags.c_contiguous and c.dtype == np.float32):
+            raise TypeError("caches must be C-contiguous fp32 numpy arrays")
+    cs = _as_f32(rope_cos) if rope_cos is not None else None
+    sn = _as_f32(rope_sin) if rope_sin is not None else None
+    if scale is None:
+        scale = 1.0 / math.sqrt(head_dim)
+    out = np.empty((num_heads, head_dim), dtype=np.float64)
+    rc = lib.oracle_decode_append(
+        _ptr(q, _f32p), _ptr(kn, _f32p), _ptr(vn, _f32p),
+        _ptr(cs, _f32p) if cs is not None else None, _ptr(sn, _f32p) if sn is not None else None,
+        _ptr(k_cache, _f32p), _ptr(v_cache, _f32p), num_heads, kv_heads, head_dim, max_seq,
+        total_seq, position, window, float(scale), _ptr(out, _f64p), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_decode_append rejected its arguments")
+    return out

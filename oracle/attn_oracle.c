@@ -23,7 +23,9 @@
  *  [P2] "soft3/glia/run/backend/honeycrisp/kernels/attention.rs", module doc
  *       (inputs, per-head formula, sliding window), `kmain` decode kernel
  *       (window start, -1e4 mask, softmax, normalise), KV_APPEND_TEMPLATE and
- *       KV_APPEND_BOTH_TEMPLATE (cache write at `position`).
+ *       KV_APPEND_BOTH_TEMPLATE (cache write at `position`),
+ *       FUSED_ROPE_KV_ATTN_TEMPLATE (rotate-half RoPE of the new key and the
+ *       query, append, decode).
  *
  * Parity pins: every function below is pinned by the `-m "not gpu"` tests
  * (closed forms, invariants, brute force, a library cross-check); none is
@@ -160,10 +162,10 @@ int oracle_prefill_causal(const float *q, const float *k, const float *v,
  * Returns 0, or -1 on an argument the definition cannot take (total_seq == 0
  * has no softmax; total_seq > max_seq reads outside the cache).
  */
-int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
-                  uint32_t num_heads, uint32_t kv_heads, uint32_t d,
-                  uint32_t max_seq, uint32_t total_seq, uint32_t window,
-                  double scale, double *out, double *weights, int nthreads) {
+static int decode_impl(const double *qd, const float *k_cache, const float *v_cache,
+                       uint32_t num_heads, uint32_t kv_heads, uint32_t d, uint32_t max_seq,
+                       uint32_t total_seq, uint32_t window, double scale, double *out,
+                       double *weights, int nthreads) {
     if (kv_heads == 0 || num_heads % kv_heads != 0 || d == 0) return -1;
     if (total_seq == 0 || total_seq > max_seq) return -1;
     const uint32_t repeat = num_heads / kv_heads;
@@ -181,13 +183,13 @@ int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
         for (uint32_t h = 0; h < num_heads; ++h) {
             if (!s) continue;
             const uint32_t kvh = h / repeat;
-            const float *qh = q + (size_t)h * d;
+            const double *qh = qd + (size_t)h * d;
             const float *kb = k_cache + (size_t)kvh * max_seq * d;
             const float *vb = v_cache + (size_t)kvh * max_seq * d;
             for (uint32_t t = 0; t < total_seq; ++t) {
                 const float *kr = kb + (size_t)t * d;
                 double dot = 0.0;
-                for (uint32_t e = 0; e < d; ++e) dot += (double)qh[e] * (double)kr[e];
+                for (uint32_t e = 0; e < d; ++e) dot += qh[e] * (double)kr[e];
                 s[t] = scale * dot;
                 if (t < ws) s[t] = -1.0e4;
             }
@@ -197,6 +199,19 @@ int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
         free(s);
     }
     return bad ? -1 : 0;
+}
+
+int oracle_decode(const float *q, const float *k_cache, const float *v_cache,
+                  uint32_t num_heads, uint32_t kv_heads, uint32_t d,
+                  uint32_t max_seq, uint32_t total_seq, uint32_t window,
+                  double scale, double *out, double *weights, int nthreads) {
+    double *qd = (double *)malloc(sizeof(double) * (size_t)num_heads * (d ? d : 1));
+    if (!qd) return -1;
+    for (size_t i = 0; i < (size_t)num_heads * d; ++i) qd[i] = (double)q[i];
+    const int rc = decode_impl(qd, k_cache, v_cache, num_heads, kv_heads, d, max_seq, total_seq,
+                               window, scale, out, weights, nthreads);
+    free(qd);
+    return rc;
 }
 
 /*
@@ -219,4 +234,65 @@ int oracle_kv_append(const float *k_src, const float *v_src, float *k_cache,
         }
     }
     return 0;
+}
+
+/*
+ * Rotate-half RoPE of one vector [P2 FUSED_ROPE_KV_ATTN_TEMPLATE]: with
+ * h = d / 2, element i pairs with i + h and
+ *   y[i]     = x[i] cos[i] - x[i+h] sin[i]
+ *   y[i + h] = x[i] sin[i] + x[i+h] cos[i]      for i in [0, h).
+ * (The page fixes d = 128, h = 64; the same rule is applied to any even d.)
+ */
+static void rope(const double *x, const float *cosv, const float *sinv, uint32_t d, double *y) {
+    const uint32_t h = d / 2;
+    for (uint32_t i = 0; i < h; ++i) {
+        const double c = (double)cosv[i], sn = (double)sinv[i];
+        y[i] = x[i] * c - x[i + h] * sn;
+        y[i + h] = x[i] * sn + x[i + h] * c;
+    }
+}
+
+/*
+ * Fused RoPE + append + decode [P2 FUSED_ROPE_KV_ATTN_TEMPLATE]:
+ *   k_cache[g, position] = rope(k_new[g])   (rounded to the fp32 cache)
+ *   v_cache[g, position] = v_new[g]
+ *   q'[h] = rope(q[h])                      (kept in double)
+ *   out = decode(q', caches, total_seq, window, scale)   (as oracle_decode)
+ * rope_cos/rope_sin = NULL: no rotation (plain append + decode).
+ * The caches are updated in place.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_decode_append(const float *q, const float *k_new, const float *v_new,
+                         const float *rope_cos, const float *rope_sin, float *k_cache,
+                         float *v_cache, uint32_t num_heads, uint32_t kv_heads, uint32_t d,
+                         uint32_t max_seq, uint32_t total_seq, uint32_t position,
+                         uint32_t window, double scale, double *out, int nthreads) {
+    if (position >= max_seq || d == 0 || (d % 2) != 0) return -1;
+    if ((rope_cos == NULL) != (rope_sin == NULL)) return -1;
+    double *tmp = (double *)malloc(sizeof(double) * d * 2);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)num_heads * d);
+    if (!tmp || !qd) {
+        free(tmp);
+        free(qd);
+        return -1;
+    }
+    for (uint32_t g = 0; g < kv_heads; ++g) {
+        for (uint32_t e = 0; e < d; ++e) tmp[e] = (double)k_new[(size_t)g * d + e];
+        if (rope_cos) rope(tmp, rope_cos, rope_sin, d, tmp + d);
+        else memcpy(tmp + d, tmp, sizeof(double) * d);
+        for (uint32_t e = 0; e < d; ++e) {
+            const size_t dst = ((size_t)g * max_seq + position) * d + e;
+            k_cache[dst] = (float)tmp[d + e];
+            v_cache[dst] = v_new[(size_t)g * d + e];
+        }
+    }
+    for (uint32_t h = 0; h < num_heads; ++h) {
+        for (uint32_t e = 0; e < d; ++e) tmp[e] = (double)q[(size_t)h * d + e];
+        if (rope_cos) rope(tmp, rope_cos, rope_sin, d, qd + (size_t)h * d);
+        else memcpy(qd + (size_t)h * d, tmp, sizeof(double) * d);
+    }
+    const int rc = decode_impl(qd, k_cache, v_cache, num_heads, kv_heads, d, max_seq, total_seq,
+                               window, scale, out, NULL, nthreads);
+    free(tmp);
+    free(qd);
+    return rc;
 }

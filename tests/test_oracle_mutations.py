@@ -35,7 +35,14 @@ MUTANTS = {
                            "const float *vr = v + (n - 1 - j) * v_row_pitch;"),
     "not_normalised": ("for (size_t j = 0; j < n; ++j) scores[j] /= l;", ""),
     "exp_base_two": ("exp(scores[j] - m)", "exp2(scores[j] - m)"),
-    "append_wrong_row": ("+ position) * d + e;", "+ position - (position > 0)) * d + e;"),
+    "append_wrong_row": ("+ position) * d + e;\n            k_cache[dst] = k_src[src];",
+                         "+ position - (position > 0)) * d + e;\n            k_cache[dst] = k_src[src];"),
+    "rope_sign_flipped": ("y[i] = x[i] * c - x[i + h] * sn;", "y[i] = x[i] * c + x[i + h] * sn;"),
+    "rope_adjacent_pairs": ("y[i + h] = x[i] * sn + x[i + h] * c;",
+                            "y[i + h] = x[i] * sn + x[i + 1 - (i + 1 == h)] * c;"),
+    "rope_query_not_rotated": ("if (rope_cos) rope(tmp, rope_cos, rope_sin, d, qd + (size_t)h * d);",
+                               "if (0) rope(tmp, rope_cos, rope_sin, d, qd + (size_t)h * d);"),
+    "fused_value_not_appended": ("v_cache[dst] = v_new[(size_t)g * d + e];", "(void)dst;"),
 }
 
 

@@ -424,3 +424,83 @@ def test_sampled_rows_match_full():
     rows = [0, 3, 17, 39]
     np.testing.assert_array_equal(oracle.prefill_causal(q, k, v, m, hq, hkv, d, qs, kvs, rows=rows),
                                   full[rows])
+
+
+# ---------------------------------------------------------------- fused RoPE + append + decode
+
+def _complex_rotate(x, theta):
+    """Rotate-half RoPE written as complex multiplication: pair (x[i], x[i+h])
+    is the complex number x[i] + 1j*x[i+h], multiplied by exp(1j*theta[i])."""
+    h = x.shape[-1] // 2
+    z = (x[..., :h].astype(np.float64) + 1j * x[..., h:].astype(np.float64)) * np.exp(1j * theta)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def test_decode_append_without_rope_is_append_then_decode():
+    """honeycrisp FUSED_ROPE_KV_ATTN_TEMPLATE with no rotation reduces to
+    KV_APPEND_BOTH_TEMPLATE followed by kmain."""
+    hq, hkv, d, S, T = 8, 2, 64, 40, 33
+    q = _rand((hq, d), 201)
+    kc, vc = _rand((hkv, S, d), 202), _rand((hkv, S, d), 203)
+    kn, vn = _rand((hkv, d), 204), _rand((hkv, d), 205)
+    k1, v1 = kc.copy(), vc.copy()
+    out = oracle.decode_append(q, kn, vn, k1, v1, hq, hkv, d, S, T, T - 1, window=8)
+    k2, v2 = kc.copy(), vc.copy()
+    oracle.kv_append(kn, vn, k2, v2, hkv, d, S, T - 1)
+    np.testing.assert_array_equal(k1, k2)
+    np.testing.assert_array_equal(v1, v2)
+    np.testing.assert_array_equal(out, oracle.decode(q, k2, v2, hq, hkv, d, S, T, window=8))
+
+
+def test_rope_quarter_turn_closed_form():
+    """cos = 0, sin = 1 rotates every pair by 90 degrees:
+    y[i] = -x[i+h], y[i+h] = x[i] (exact in fp32)."""
+    hq, hkv, d, S = 2, 1, 32, 4
+    q = _rand((hq, d), 211)
+    kc, vc = _rand((hkv, S, d), 212), _rand((hkv, S, d), 213)
+    kn, vn = _rand((hkv, d), 214), _rand((hkv, d), 215)
+    cos = np.zeros(d // 2, np.float32)
+    sin = np.ones(d // 2, np.float32)
+    oracle.decode_append(q, kn, vn, kc, vc, hq, hkv, d, S, S, 2, rope_cos=cos, rope_sin=sin)
+    np.testing.assert_array_equal(kc[0, 2], np.concatenate([-kn[0, d // 2:], kn[0, :d // 2]]))
+    np.testing.assert_array_equal(vc[0, 2], vn[0])
+
+
+def test_rope_matches_complex_rotation_and_keeps_norms():
+    hkv, d, S = 3, 64, 8
+    theta = np.random.default_rng(7).uniform(-3, 3, d // 2)
+    cos, sin = np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
+    q = _rand((6, d), 221)
+    kc, vc = _rand((hkv, S, d), 222), _rand((hkv, S, d), 223)
+    kn, vn = _rand((hkv, d), 224), _rand((hkv, d), 225)
+    oracle.decode_append(q, kn, vn, kc, vc, 6, hkv, d, S, S, 5, rope_cos=cos, rope_sin=sin)
+    # the fp32 tables are not exactly on the unit circle: rotate by their angle
+    # and scale by their radius
+    th32 = np.arctan2(sin.astype(np.float64), cos.astype(np.float64))
+    rad = np.hypot(cos.astype(np.float64), sin.astype(np.float64))
+    ref = _complex_rotate(kn, th32) * np.concatenate([rad, rad])
+    np.testing.assert_allclose(kc[:, 5], ref, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(np.linalg.norm(kc[:, 5].astype(np.float64), axis=1),
+                               np.linalg.norm(kn.astype(np.float64), axis=1), rtol=1e-6)
+
+
+def test_rope_same_angle_leaves_scores_unchanged():
+    """Rotating the query and every key by the same angles keeps each q.k
+    (RoPE is a rotation): prerotate the old keys with the complex form, append
+    a rotated key, and the result equals plain append + decode on the
+    unrotated vectors."""
+    hq, hkv, d, S, T = 4, 2, 32, 12, 12
+    theta = np.random.default_rng(3).uniform(-3, 3, d // 2)
+    cos, sin = np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
+    th = np.arctan2(sin.astype(np.float64), cos.astype(np.float64))
+    q = _rand((hq, d), 231)
+    kc, vc = _rand((hkv, S, d), 232), _rand((hkv, S, d), 233)
+    kn, vn = _rand((hkv, d), 234), _rand((hkv, d), 235)
+    k_rot = _complex_rotate(kc, th).astype(np.float32)
+    v1 = vc.copy()
+    got = oracle.decode_append(q, kn, vn, k_rot, v1, hq, hkv, d, S, T, T - 1, rope_cos=cos,
+                               rope_sin=sin)
+    k_plain = _complex_rotate(_complex_rotate(kc, th).astype(np.float32), -th).astype(np.float32)
+    v2 = vc.copy()
+    ref = oracle.decode_append(q, kn, vn, k_plain, v2, hq, hkv, d, S, T, T - 1)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=5e-5)
