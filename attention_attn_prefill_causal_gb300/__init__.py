@@ -19,7 +19,8 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "ATTN_ERR_RANGE", "ATTN_PREC_FP32", "ATTN_PREC_FP16", "ATTN_PREC_BF16",
     "AttnError", "lib", "library_path", "attn_prefill_causal", "attn_prefill_workspace_size",
-    "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc", "kv_append", "attn_status_string",
+    "attn_decode", "attn_decode_workspace_size", "attn_decode_append", "attn_decode_noalloc",
+    "kv_append", "attn_status_string",
     "attn_last_error_string", "attn_get_device_status", "attn_selftest_wait_timeout",
     "exported_symbols",
 ]
@@ -47,6 +48,8 @@ _SIGS = {
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _f32, _vp, _sz,
                          _vp]),
     "attn_decode_workspace_size": (_sz, [_u32, _u32, _u32, _u32, _u32]),
+    "attn_decode_append": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32,
+                                _u32, _u32, _u32, _f32, _vp, _sz, _vp]),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _f32,
                                  _vp]),
     "kv_append": (_i, [_vp, _vp, _vp, _vp, _u32, _u32, _u32, _u32, _vp]),
@@ -98,11 +101,13 @@ def _check(status: int, where: str, check: bool) -> int:
 
 
 def _workspace(nbytes: int, like, workspace):
+    """A zeroed device workspace (the decode workspace starts with arrival
+    counters that must be zero before its first use)."""
     if workspace is not None or nbytes == 0:
         return workspace
     import torch
     dev = like.device if hasattr(like, "device") else torch.device("cuda", torch.cuda.current_device())
-    return torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
 
 def attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim, precision=ATTN_PREC_FP16):
@@ -142,6 +147,23 @@ def attn_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq
                          head_dim, max_seq, total_seq, window, float(scale), _ptr(workspace),
                          workspace_bytes, _stream(stream))
     return _check(st, "attn_decode", check)
+
+
+def attn_decode_append(q, k_new, v_new, k_cache, v_cache, out, num_heads, kv_heads, head_dim,
+                       max_seq, total_seq, position, window=0, scale=0.0, rope_cos=None,
+                       rope_sin=None, workspace=None, workspace_bytes=None, stream=None,
+                       check=True):
+    """Fused (RoPE +) append + decode (C: attn_decode_append)."""
+    need = attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window)
+    workspace = _workspace(need, q, workspace)
+    if workspace_bytes is None:
+        workspace_bytes = (workspace.numel() * workspace.element_size()
+                           if hasattr(workspace, "numel") else need)
+    st = lib.attn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin),
+                                _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, kv_heads,
+                                head_dim, max_seq, total_seq, position, window, float(scale),
+                                _ptr(workspace), workspace_bytes, _stream(stream))
+    return _check(st, "attn_decode_append", check)
 
 
 def attn_decode_noalloc(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq,

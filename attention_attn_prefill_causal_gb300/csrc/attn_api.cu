@@ -153,10 +153,12 @@ size_t attn_decode_workspace_size(uint32_t num_heads, uint32_t kv_heads, uint32_
         .workspace_bytes;
 }
 
-attn_status_t attn_decode(const float* q, const float* k_cache, const float* v_cache,
-                          float* out, uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
-                          uint32_t max_seq, uint32_t total_seq, uint32_t window, float scale,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+// Shared validation of the decode entry points; fills the plan.
+static attn_status_t check_decode(const float* q, const float* k_cache, const float* v_cache,
+                                  const float* out, uint32_t num_heads, uint32_t kv_heads,
+                                  uint32_t head_dim, uint32_t max_seq, uint32_t total_seq,
+                                  uint32_t window, float scale, const void* workspace,
+                                  size_t workspace_bytes, DecodePlan* plan) {
     if (!q || !k_cache || !v_cache || !out) return ATTN_ERR_INVALID_ARG;
     if (num_heads == 0 || kv_heads == 0 || num_heads % kv_heads != 0) return ATTN_ERR_INVALID_ARG;
     if (head_dim == 0 || head_dim % 32 != 0) return ATTN_ERR_INVALID_ARG;
@@ -165,17 +167,72 @@ attn_status_t attn_decode(const float* q, const float* k_cache, const float* v_c
         return ATTN_ERR_INVALID_ARG;
     if (!(scale >= 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (head_dim != 32 && head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
-    const DecodePlan plan =
-        make_decode_plan(num_heads, kv_heads, head_dim, total_seq, window, device_sm_count());
-    if (!workspace || workspace_bytes < plan.workspace_bytes) return ATTN_ERR_INVALID_ARG;
+    *plan = make_decode_plan(num_heads, kv_heads, head_dim, total_seq, window, device_sm_count());
+    if (!workspace || workspace_bytes < plan->workspace_bytes) return ATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
-    float* part_o = static_cast<float*>(workspace);
-    float* part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                              (plan.part_o_floats * 4 + 255) / 256 * 256);
-    return record_cuda_error(launch_decode(q, k_cache, v_cache, out, num_heads, kv_heads,
-                                           head_dim, max_seq, total_seq, plan,
-                                           resolve_scale(scale, head_dim), part_o, part_ml,
-                                           static_cast<cudaStream_t>(stream)));
+    return ATTN_OK;
+}
+
+attn_status_t attn_decode(const float* q, const float* k_cache, const float* v_cache,
+                          float* out, uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
+                          uint32_t max_seq, uint32_t total_seq, uint32_t window, float scale,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    DecodePlan plan;
+    const attn_status_t st = check_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim,
+                                          max_seq, total_seq, window, scale, workspace,
+                                          workspace_bytes, &plan);
+    if (st != ATTN_OK) return st;
+    DecodeCall c{};
+    c.q = q;
+    c.k_cache = k_cache;
+    c.v_cache = v_cache;
+    c.out = out;
+    c.num_heads = num_heads;
+    c.kv_heads = kv_heads;
+    c.head_dim = head_dim;
+    c.max_seq = max_seq;
+    c.total_seq = total_seq;
+    c.scale = resolve_scale(scale, head_dim);
+    return record_cuda_error(
+        launch_decode(c, plan, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_decode_append(const float* q, const float* k_new, const float* v_new,
+                                 const float* rope_cos, const float* rope_sin, float* k_cache,
+                                 float* v_cache, float* out, uint32_t num_heads,
+                                 uint32_t kv_heads, uint32_t head_dim, uint32_t max_seq,
+                                 uint32_t total_seq, uint32_t position, uint32_t window,
+                                 float scale, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+    if (!k_new || !v_new) return ATTN_ERR_INVALID_ARG;
+    if ((rope_cos == nullptr) != (rope_sin == nullptr)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return ATTN_ERR_INVALID_ARG;
+    if (position >= max_seq) return ATTN_ERR_INVALID_ARG;
+    DecodePlan plan;
+    const attn_status_t st = check_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim,
+                                          max_seq, total_seq, window, scale, workspace,
+                                          workspace_bytes, &plan);
+    if (st != ATTN_OK) return st;
+    DecodeCall c{};
+    c.q = q;
+    c.k_cache = k_cache;
+    c.v_cache = v_cache;
+    c.k_cache_w = k_cache;
+    c.v_cache_w = v_cache;
+    c.k_new = k_new;
+    c.v_new = v_new;
+    c.rope_cos = rope_cos;
+    c.rope_sin = rope_sin;
+    c.out = out;
+    c.num_heads = num_heads;
+    c.kv_heads = kv_heads;
+    c.head_dim = head_dim;
+    c.max_seq = max_seq;
+    c.total_seq = total_seq;
+    c.position = position;
+    c.scale = resolve_scale(scale, head_dim);
+    return record_cuda_error(
+        launch_decode(c, plan, workspace, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t kv_append(const float* k_src, const float* v_src, float* k_cache, float* v_cache,

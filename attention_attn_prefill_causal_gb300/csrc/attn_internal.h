@@ -31,9 +31,11 @@ void set_last_error(const char* msg);
 struct DecodePlan {
     uint32_t window_start;
     uint32_t rows_live;
-    uint32_t chunk;      // live rows per split
-    uint32_t n_splits;   // splits per KV head
-    uint32_t n_hgroups;  // query-head groups of <= 8 heads per KV head
+    uint32_t heads_per_pass;  // query heads per CTA (1, 2, 4 or 8)
+    uint32_t n_hgroups;       // query-head groups per KV head
+    uint32_t chunk;           // live rows per CTA
+    uint32_t rows_per_warp;   // rows per warp: ceil(chunk / warps per CTA)
+    uint32_t n_splits;        // CTAs (row chunks) per KV head group
     size_t part_o_floats;
     size_t part_ml_floats;
     size_t workspace_bytes;
@@ -41,10 +43,24 @@ struct DecodePlan {
 DecodePlan make_decode_plan(uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
                             uint32_t total_seq, uint32_t window, int sm_count);
 
-cudaError_t launch_decode(const float* q, const float* k_cache, const float* v_cache,
-                          float* out, uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
-                          uint32_t max_seq, uint32_t total_seq, const DecodePlan& plan,
-                          float scale, float* part_o, float* part_ml, cudaStream_t stream);
+// One decode call; k_new == nullptr means no append (plain decode).
+struct DecodeCall {
+    const float* q;
+    const float* k_cache;
+    const float* v_cache;
+    float* k_cache_w;
+    float* v_cache_w;
+    const float* k_new;
+    const float* v_new;
+    const float* rope_cos;
+    const float* rope_sin;
+    float* out;
+    uint32_t num_heads, kv_heads, head_dim, max_seq, total_seq, position;
+    float scale;
+};
+
+cudaError_t launch_decode(const DecodeCall& call, const DecodePlan& plan, void* workspace,
+                          cudaStream_t stream);
 
 cudaError_t launch_kv_append(const float* k_src, const float* v_src, float* k_cache,
                              float* v_cache, uint32_t kv_heads, uint32_t head_dim,

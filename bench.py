@@ -1,8 +1,9 @@
 """Benchmark of the attention hot path on GB300: one JSON line on rank 0.
 
 Headline workload (the decode configuration): 12 query heads over 2 KV heads,
-head_dim 128, a 4096-row cache, no window.  One step = kv_append of the new
-K/V row at position total_seq-1 followed by attn_decode over all 4096 rows.
+head_dim 128, a 4096-row cache, no window.  One step = append of the new
+K/V row at position total_seq-1 and decode over all 4096 rows, as one fused
+kernel (attn_decode_append).
 Metric value = algorithmic K+V bytes (2 * kv_heads * total_seq * head_dim * 4)
 per step x steps / device time, in GB/s.  The caches rotate over enough
 replicas that every step reads them cold from HBM (the replicas together
@@ -209,19 +210,21 @@ class DecodeBench:
         self.out = torch.empty(shape.num_heads, shape.head_dim, device=device)
         ws = attn.attn_decode_workspace_size(shape.num_heads, shape.kv_heads, shape.head_dim,
                                              shape.total_seq, shape.window)
-        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(ws, dtype=torch.uint8, device=device)  # counters start at zero
         self.pos = shape.total_seq - 1
-        self.launches_per_step = 3  # kv_append, split, combine
+        self.launches_per_step = 1  # one fused append + decode kernel
 
     def step(self, i, stream, append=True):
         c, a = self.c, self.attn
         r = i % self.R
         if append:
-            a.kv_append(self.kn, self.vn, self.kc[r], self.vc[r], c.kv_heads, c.head_dim,
-                        c.max_seq, self.pos, stream=stream)
-        a.attn_decode(self.q, self.kc[r], self.vc[r], self.out, c.num_heads, c.kv_heads,
-                      c.head_dim, c.max_seq, c.total_seq, window=c.window, workspace=self.ws,
-                      stream=stream)
+            a.attn_decode_append(self.q, self.kn, self.vn, self.kc[r], self.vc[r], self.out,
+                                 c.num_heads, c.kv_heads, c.head_dim, c.max_seq, c.total_seq,
+                                 self.pos, window=c.window, workspace=self.ws, stream=stream)
+        else:
+            a.attn_decode(self.q, self.kc[r], self.vc[r], self.out, c.num_heads, c.kv_heads,
+                          c.head_dim, c.max_seq, c.total_seq, window=c.window,
+                          workspace=self.ws, stream=stream)
 
     def graphs(self, stream, append=True):
         def chunk():
@@ -504,10 +507,10 @@ def our_arm(args):
     per_decode = dsecs / n_dec
     achieved = bytes_step / per_decode / 1e9
     hbm = float(peaks["hbm_gbs"])
-    traffic = traffic_for("attn_decode", ["decode.cu"])
+    traffic = traffic_for("decode_kernel", ["decode.cu"])
 
     # End to end through the Python API: per step, H2D of q, k_new, v_new from
-    # pinned host memory, kv_append + attn_decode, D2H of the output.
+    # pinned host memory, fused append + decode, D2H of the output.
     q, kc, vc, kn, vn = db.host
     hq, hkn, hvn = q.pin_memory(), kn.pin_memory(), vn.pin_memory()
     hout = torch.empty(shape.num_heads, shape.head_dim).pin_memory()
@@ -557,7 +560,8 @@ def our_arm(args):
                        "kv_heads": shape.kv_heads, "head_dim": shape.head_dim,
                        "max_seq": shape.max_seq, "total_seq": shape.total_seq,
                        "window": shape.window,
-                       "step": "kv_append at total_seq-1 + attn_decode (CUDA-graph replays)",
+                       "step": "attn_decode_append: append at total_seq-1 + decode, one kernel "
+                               "(CUDA-graph replays)",
                        "l2": f"inputs larger than L2: {db.R} rotating cache replicas "
                              f"({db.R * 2 * shape.kv_heads * shape.max_seq * shape.head_dim * 4 // 2**20} MiB)",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -565,7 +569,7 @@ def our_arm(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
                          "peak_source": f"hbm_gbs ({peak_src})",
-                         "kernel": "attn_decode call (decode_split_kernel + decode_combine_kernel)",
+                         "kernel": "decode_kernel (attn_decode call, one launch)",
                          "ms_per_launch": round(per_decode * 1e3, 5)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e_bytes / e_max / 1e9, 3), "unit": "GB/s",

@@ -126,9 +126,36 @@ attn_status_t attn_decode(const float* q, const float* k_cache, const float* v_c
 
 /* Bytes of workspace attn_decode needs.  Depends on the arguments and on the
  * SM count of the current device (152 is assumed when no device is
- * visible). */
+ * visible).  Its contents need no initialisation.  Calls that overlap on the
+ * GPU need separate workspaces. */
 size_t attn_decode_workspace_size(uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
                                   uint32_t total_seq, uint32_t window);
+
+/*
+ * attn_decode_append -- append one K/V row (optionally rotated) and decode,
+ * in one launch.
+ *
+ * Defined by "soft3/glia/run/backend/honeycrisp/kernels/attention.rs",
+ * FUSED_ROPE_KV_ATTN_TEMPLATE: the new key is rotated with rotate-half RoPE
+ * (element d pairs with d + head_dim/2: x'[d] = x[d]cos[d] - x[d+h]sin[d],
+ * x'[d+h] = x[d]sin[d] + x[d+h]cos[d], h = head_dim/2) and written to
+ * k_cache[g, position]; v_new is copied to v_cache[g, position]; the query is
+ * rotated the same way; then the decode of attn_decode runs over
+ * [0, total_seq) with the window, seeing the appended row.
+ *
+ *   k_new, v_new        : [kv_heads, head_dim] fp32
+ *   rope_cos, rope_sin  : [head_dim/2] fp32 tables for this position, or both
+ *                         NULL for no rotation (plain append + decode)
+ *   position            : row written; < max_seq (normally total_seq - 1)
+ * Other arguments, workspace rules and validation as attn_decode.
+ */
+attn_status_t attn_decode_append(const float* q, const float* k_new, const float* v_new,
+                                 const float* rope_cos, const float* rope_sin, float* k_cache,
+                                 float* v_cache, float* out, uint32_t num_heads,
+                                 uint32_t kv_heads, uint32_t head_dim, uint32_t max_seq,
+                                 uint32_t total_seq, uint32_t position, uint32_t window,
+                                 float scale, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /*
  * attn_decode_noalloc -- attn_decode without a caller workspace.  The pages
@@ -138,8 +165,8 @@ size_t attn_decode_workspace_size(uint32_t num_heads, uint32_t kv_heads, uint32_
  * input and output pointers, a loop where allocation is not allowed).
  *
  * Same arguments, results and validation as attn_decode, minus the
- * workspace.  The split partials live in a fixed 4 MiB device array inside
- * libattn (resident on every GPU that loads the library, until exit); sizes
+ * workspace.  Its workspace (the per-chunk partials) is a fixed 4 MiB
+ * device array inside libattn (resident on every GPU that loads the library, until exit); sizes
  * whose attn_decode_workspace_size() exceeds 4 MiB are rejected with
  * ATTN_ERR_UNSUPPORTED and a message in attn_last_error_string().  The call
  * allocates nothing.  Its first call on a device looks up the array's device

@@ -328,3 +328,86 @@ def test_bounded_wait_times_out_and_context_survives(attn):
     assert attn.attn_selftest_wait_timeout(1000) == attn.ATTN_ERR_TIMEOUT
     assert attn.attn_get_device_status() == attn.ATTN_OK
     _check_prefill(attn, 200, 2, 1, 128, FP16, seed=1)
+
+
+# ------------------------------------------------------------------ fused (RoPE +) append + decode
+
+def _rope_tables(d, seed):
+    theta = np.random.default_rng(seed).uniform(-3.0, 3.0, d // 2)
+    return np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
+
+
+@pytest.mark.parametrize("rope", [False, True])
+@pytest.mark.parametrize("hq,hkv,d,S,T,W", [(12, 2, 128, 4096, 4096, 0),
+                                            (32, 8, 128, 32768, 32768, 4096),
+                                            (8, 8, 64, 300, 257, 0),
+                                            (24, 2, 32, 1000, 1000, 100)])
+def test_decode_append_matches_oracle(attn, rope, hq, hkv, d, S, T, W):
+    q, kc, vc, kn, vn = workloads.decode_inputs(hq, hkv, d, S, seed=hq + d + T, append=True)
+    cos = sin = None
+    if rope:
+        cos, sin = _rope_tables(d, T)
+    dk, dv = kc.cuda(), vc.cuda()
+    buf, out = guarded_empty(hq * d)
+    pos = T - 1
+    attn.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), dk, dv, out, hq, hkv, d, S, T, pos,
+                            window=W,
+                            rope_cos=torch.from_numpy(cos).cuda() if rope else None,
+                            rope_sin=torch.from_numpy(sin).cuda() if rope else None)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK and guards_intact(buf)
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    ref = oracle.decode_append(q.numpy(), kn.numpy(), vn.numpy(), kh, vh, hq, hkv, d, S, T, pos,
+                               window=W, rope_cos=cos, rope_sin=sin)
+    np.testing.assert_allclose(dk[:, pos].cpu().numpy(), kh[:, pos], rtol=0, atol=2e-6)
+    np.testing.assert_array_equal(dv[:, pos].cpu().numpy(), vh[:, pos])
+    amax, rel = compare(out.view(hq, d).cpu().numpy(), ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
+
+
+def test_decode_append_position_inside_the_cache(attn):
+    """An append in the middle of the attended range replaces that row."""
+    hq, hkv, d, S, T = 8, 2, 128, 512, 500
+    q, kc, vc, kn, vn = workloads.decode_inputs(hq, hkv, d, S, seed=77, append=True)
+    dk, dv = kc.cuda(), vc.cuda()
+    out = torch.empty(hq, d, device="cuda")
+    attn.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), dk, dv, out, hq, hkv, d, S, T, 123)
+    torch.cuda.synchronize()
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    ref = oracle.decode_append(q.numpy(), kn.numpy(), vn.numpy(), kh, vh, hq, hkv, d, S, T, 123)
+    amax, rel = compare(out.cpu().numpy(), ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+def test_decode_append_equals_unfused_append_then_decode(attn):
+    """The fused entry point and kv_append + attn_decode agree to fp32 rounding."""
+    c = workloads.DECODE_32K_WINDOW
+    q, kc, vc, kn, vn = workloads.shape_inputs(c)
+    pos = c.total_seq - 1
+    k1, v1, k2, v2 = kc.cuda(), vc.cuda(), kc.cuda(), vc.cuda()
+    o1 = torch.empty(c.num_heads, c.head_dim, device="cuda")
+    o2 = torch.empty_like(o1)
+    attn.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), k1, v1, o1, c.num_heads, c.kv_heads,
+                            c.head_dim, c.max_seq, c.total_seq, pos, window=c.window)
+    attn.kv_append(kn.cuda(), vn.cuda(), k2, v2, c.kv_heads, c.head_dim, c.max_seq, pos)
+    attn.attn_decode(q.cuda(), k2, v2, o2, c.num_heads, c.kv_heads, c.head_dim, c.max_seq,
+                     c.total_seq, window=c.window)
+    torch.cuda.synchronize()
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    assert (o1 - o2).abs().max().item() <= 1e-6
+
+
+def test_decode_workspace_reuse(attn):
+    """One workspace, never cleared, serves many calls of different shapes."""
+    ws = torch.full((8 << 20,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN garbage
+    for (hq, hkv, d, S, T, W) in [(12, 2, 128, 4096, 4096, 0), (32, 8, 128, 8192, 8000, 1000),
+                                  (12, 2, 128, 4096, 4096, 0), (4, 1, 64, 100, 3, 0),
+                                  (64, 8, 128, 20000, 20000, 0)]:
+        q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=T)
+        out = torch.empty(hq, d, device="cuda")
+        attn.attn_decode(q.cuda(), kc.cuda(), vc.cuda(), out, hq, hkv, d, S, T, window=W,
+                         workspace=ws)
+        torch.cuda.synchronize()
+        ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, W)
+        amax, rel = compare(out.cpu().numpy(), ref)
+        assert amax <= FP32_ABS and rel <= FP32_REL
