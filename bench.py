@@ -2,8 +2,9 @@
 
 Headline workload (the decode configuration): 12 query heads over 2 KV heads,
 head_dim 128, a 4096-row cache, no window.  One step = append of the new
-K/V row at position total_seq-1 and decode over all 4096 rows, as one fused
-kernel (attn_decode_append).
+K/V row at position total_seq-1 and decode over all 4096 rows
+(attn_decode_append: the decode kernel with the append fused, and its
+combine kernel).
 Metric value = algorithmic K+V bytes (2 * kv_heads * total_seq * head_dim * 4)
 per step x steps / device time, in GB/s.  The caches rotate over enough
 replicas that every step reads them cold from HBM (the replicas together
@@ -212,7 +213,7 @@ class DecodeBench:
                                              shape.total_seq, shape.window)
         self.ws = torch.zeros(ws, dtype=torch.uint8, device=device)  # counters start at zero
         self.pos = shape.total_seq - 1
-        self.launches_per_step = 1  # one fused append + decode kernel
+        self.launches_per_step = 2  # fused append + decode kernel, PDL combine kernel
 
     def step(self, i, stream, append=True):
         c, a = self.c, self.attn
@@ -350,7 +351,7 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
     tflops = flops / per_call / 1e12
     peak_key = "bf16_tflops_sustained" if secs > 1.0 else "bf16_tflops"
     peak = float(peaks[peak_key])
-    traffic = traffic_for("prefill_tc_kernel", ["prefill_tc.cu", "sm103_ptx.cuh"])
+    traffic = traffic_for(f"prefill_tc_kernel:{shape.name}", ["prefill_tc.cu", "sm103_ptx.cuh"])
 
     # end to end through the Python API with host buffers (pinned)
     q, k, v = pb.host
@@ -469,6 +470,13 @@ def our_arm(args):
 
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=device)
+    if args.only in ("prefill_2k", "prefill_16k"):
+        # Profiling aid: one prefill workload alone (no headline line).
+        ps = workloads.PREFILL_2K if args.only == "prefill_2k" else workloads.PREFILL_16K
+        res = bench_prefill(attn, ps, device, stream, 200 if ps.m <= 4096 else 20, peaks, peak_src)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "prefill": [res]}), flush=True)
+        return 0
     shape = workloads.DECODE_4K
     db = DecodeBench(attn, shape, device)
     err = db.check()
@@ -507,7 +515,7 @@ def our_arm(args):
     per_decode = dsecs / n_dec
     achieved = bytes_step / per_decode / 1e9
     hbm = float(peaks["hbm_gbs"])
-    traffic = traffic_for("decode_kernel", ["decode.cu"])
+    traffic = traffic_for(f"attn_decode:{shape.name}", ["decode.cu"])
 
     # End to end through the Python API: per step, H2D of q, k_new, v_new from
     # pinned host memory, fused append + decode, D2H of the output.
@@ -533,7 +541,7 @@ def our_arm(args):
     e_max, e_bytes = aggregate(e_secs, bytes_step * e_steps, ws)
 
     prefill = []
-    if not args.no_prefill:
+    if not args.no_prefill and args.only == "all":
         for ps in (workloads.PREFILL_2K, workloads.PREFILL_16K):
             calls = 200 if ps.m <= 4096 else 20
             prefill.append(bench_prefill(attn, ps, device, stream, calls, peaks, peak_src))
@@ -560,8 +568,8 @@ def our_arm(args):
                        "kv_heads": shape.kv_heads, "head_dim": shape.head_dim,
                        "max_seq": shape.max_seq, "total_seq": shape.total_seq,
                        "window": shape.window,
-                       "step": "attn_decode_append: append at total_seq-1 + decode, one kernel "
-                               "(CUDA-graph replays)",
+                       "step": "attn_decode_append: append at total_seq-1 + decode (decode "
+                               "kernel + PDL combine kernel), CUDA-graph replays",
                        "l2": f"inputs larger than L2: {db.R} rotating cache replicas "
                              f"({db.R * 2 * shape.kv_heads * shape.max_seq * shape.head_dim * 4 // 2**20} MiB)",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -569,7 +577,7 @@ def our_arm(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
                          "peak_source": f"hbm_gbs ({peak_src})",
-                         "kernel": "decode_kernel (attn_decode call, one launch)",
+                         "kernel": "attn_decode call: decode_kernel + decode_combine_kernel (PDL)",
                          "ms_per_launch": round(per_decode * 1e3, 5)},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e_bytes / e_max / 1e9, 3), "unit": "GB/s",
@@ -597,6 +605,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "decode", "prefill_2k", "prefill_16k"],
+                    default="all", help="profiling aid: run one workload only")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
