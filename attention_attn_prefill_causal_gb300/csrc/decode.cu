@@ -310,10 +310,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
                 const bool live = base + u < r1;
 #pragma unroll
                 for (int hp = 0; hp < GP / 2; ++hp) {
-                    const float2* qp = reinterpret_cast<const float2*>(sq) + hp * D + lane * V;
                     float2 acc = make_float2(0.f, 0.f);
+                    {
+                        const float2* qp = reinterpret_cast<const float2*>(sq) + hp * D + lane * V;
 #pragma unroll
-                    for (int e = 0; e < V; ++e) acc = __ffma2_rn(qp[e], kd[e], acc);
+                        for (int e = 0; e < V; ++e) acc = __ffma2_rn(qp[e], kd[e], acc);
+                    }
                     part[u * GP + 2 * hp] = live ? acc.x : 0.f;
                     part[u * GP + 2 * hp + 1] = live ? acc.y : 0.f;
                 }
@@ -460,13 +462,13 @@ struct CombineArgs {
 };
 
 // Combine kernel: one CTA per (query head, 32 elements of head_dim); lane =
-// element, warp w takes the partials w, w + 8, ... in batches whose loads are
-// all issued before they are used.  Launched as a programmatic dependent of
+// element, warp w takes the partials w, w + 16, ... in batches whose loads
+// are all issued before they are used (one round trip for up to 256).  Launched as a programmatic dependent of
 // the decode kernel: it starts early and waits for that grid's results.
 template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const CombineArgs a) {
-    constexpr int kCW = 8;     // warps
-    constexpr int kBatch = 8;  // partials per warp per batch
+__global__ void __launch_bounds__(512) decode_combine_kernel(const CombineArgs a) {
+    constexpr int kCW = 16;     // warps
+    constexpr int kBatch = 16;  // partials per warp per batch (256 per round trip)
     __shared__ float sm_m[kCW], sm_l[kCW];
     __shared__ float sm_o[kCW][32];
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -558,7 +560,7 @@ cudaError_t launch_gp(const DecodeArgs& a, const DecodePlan& plan, uint32_t kv_h
     c.position = a.position;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_heads, D / 32, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(512, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
