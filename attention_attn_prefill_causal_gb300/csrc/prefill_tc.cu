@@ -303,12 +303,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (any_fail) { ok = false; break; }
             tc_fence_after();
             float s[kBN];
+            {
+                uint32_t r[kBN];
+                tmem_ld128_sync(t_s, r);
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32_sync(t_s + c * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+                for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
             }
             if (j + 1 == nkv) {  // diagonal tile: keys above the row are not attended
                 const uint32_t key0 = j * kBN;
@@ -316,9 +315,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (int c = 0; c < kBN; ++c)
                     if (key0 + c > row) s[c] = -CUDART_INF_F;
             }
-            float mx = s[0];
+            // Row max as 8 independent chains (a single 128-long chain of
+            // dependent max operations would sit on the ping-pong's critical path).
+            float mx8[8];
 #pragma unroll
-            for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+            for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < kBN; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], s[c]);
+            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_new = mx * scale_log2;
             float corr = 1.f;
             bool rescale = false;
@@ -328,19 +333,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 m_used = m_new;
             }
             const float neg_m = -m_used;
-            float rowsum = 0.f;
+            // exponent arguments two at a time (packed fp32x2), row sum as four
+            // independent packed accumulators
+            const float2 sc2 = make_float2(scale_log2, scale_log2);
+            const float2 nm2 = make_float2(neg_m, neg_m);
+            float2 acc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2(fmaf(s[c * 32 + 2 * i], scale_log2, neg_m));
-                    const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], scale_log2, neg_m));
-                    rowsum += p0 + p1;
+                    const float2 x = __ffma2_rn(
+                        make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2, nm2);
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
+                    acc[i % 4] = __fadd2_rn(acc[i % 4], make_float2(p0, p1));
                     pk[i] = pack_half2(p0, p1, BF16);
                 }
                 tmem_st16(t_s + c * 16, pk);
             }
+            const float rowsum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
+                                 ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             l_sum = fmaf(l_sum, corr, rowsum);
             if (__any_sync(0xffffffffu, rescale)) {
                 const float f = rescale ? corr : 1.f;

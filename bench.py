@@ -394,6 +394,52 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
     }
 
 
+# ---------------------------------------------------------------- layer stack (launch cost)
+
+def bench_layer_stack(attn, shape, device, stream, layers=28, reps=5):
+    """A prefill pass over an L-layer stack (the pages' 28-layer model
+    context): every layer runs attn_prefill_causal on its own Q/K/V.
+    Timed as eager launches from Python and as one CUDA-graph replay; the
+    difference is the host launch cost a graph removes."""
+    q, k, v = workloads.shape_inputs(shape)
+    qs = [q.to(device) for _ in range(layers)]
+    ks = [k.to(device) for _ in range(layers)]
+    vs = [v.to(device) for _ in range(layers)]
+    os_ = [torch.empty_like(qs[0]) for _ in range(layers)]
+    ws = torch.empty(attn.attn_prefill_workspace_size(shape.m, shape.num_q_heads,
+                                                      shape.num_kv_heads, shape.head_dim),
+                     dtype=torch.uint8, device=device)
+    c = shape
+
+    def one_pass():
+        for i in range(layers):
+            attn.attn_prefill_causal(qs[i], ks[i], vs[i], os_[i], c.m, c.num_q_heads,
+                                     c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride,
+                                     workspace=ws, stream=stream)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps, (time.perf_counter() - t0) * 1e3 / reps
+    eager_ms, eager_host_ms = timed(one_pass)
+    g = make_graph(one_pass, stream)
+    graph_ms, graph_host_ms = timed(g.replay)
+    return {"workload": f"{layers} layers x {shape.name}", "layers": layers,
+            "launches_per_pass": 2 * layers,
+            "eager_ms_per_pass": round(eager_ms, 4), "graph_ms_per_pass": round(graph_ms, 4),
+            "eager_host_ms_per_pass": round(eager_host_ms, 4),
+            "graph_host_ms_per_pass": round(graph_host_ms, 4)}
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 
 def cpu_baseline_decode(shape, budget_s=10.0, max_steps=2000):
@@ -546,6 +592,10 @@ def our_arm(args):
             calls = 200 if ps.m <= 4096 else 20
             prefill.append(bench_prefill(attn, ps, device, stream, calls, peaks, peak_src))
 
+    layer_stack = None
+    if not args.no_prefill and args.only == "all":
+        layer_stack = bench_layer_stack(attn, workloads.PREFILL_2K, device, stream)
+
     status = attn.attn_get_device_status()
     if status != attn.ATTN_OK:
         raise SystemExit(f"device status after the run: {attn.attn_status_string(status)}")
@@ -589,6 +639,7 @@ def our_arm(args):
             "clocks": clocks,
             "parity_max_abs_err": err,
             "prefill": prefill,
+            "layer_stack": layer_stack,
         }
         print(json.dumps(line), flush=True)
     barrier(ws)

@@ -411,3 +411,41 @@ def test_decode_workspace_reuse(attn):
         ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, W)
         amax, rel = compare(out.cpu().numpy(), ref)
         assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+# ------------------------------------------------------------------ autoregressive loop
+
+@pytest.mark.parametrize("prec", [FP32, FP16])
+def test_autoregressive_steps_match_prefill_rows(attn, prec):
+    """Prefill a prompt, then run decode steps that append each new token's
+    K/V row and attend to the cache: step t must reproduce row P+t of a causal
+    prefill over the whole sequence (honeycrisp KV_APPEND + kmain against
+    prefill_fused.rs).  Both sides run on the GPU; the oracle checks them."""
+    P, N, hq, hkv, d = 200, 24, 8, 2, 128
+    M = P + N
+    q, k, v = workloads.prefill_inputs(M, hq * d, hkv * d, seed=901)
+    full = _run_prefill(attn, q, k, v, M, hq, hkv, d, hq * d, hkv * d, prec)
+    # cache holding the prompt rows
+    kc = torch.zeros(hkv, M, d, device="cuda")
+    vc = torch.zeros(hkv, M, d, device="cuda")
+    kc[:, :P] = k[:P].view(P, hkv, d).transpose(0, 1).cuda()
+    vc[:, :P] = v[:P].view(P, hkv, d).transpose(0, 1).cuda()
+    out = torch.empty(hq, d, device="cuda")
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), M, hq, hkv, d, hq * d, hkv * d,
+                                rows=list(range(P, M)))
+    for t in range(N):
+        pos = P + t
+        qt = q[pos].view(hq, d).cuda()
+        kt = k[pos].view(hkv, d).cuda()
+        vt = v[pos].view(hkv, d).cuda()
+        if t % 2 == 0:   # fused entry point on even steps, separate calls on odd steps
+            attn.attn_decode_append(qt, kt, vt, kc, vc, out, hq, hkv, d, M, pos + 1, pos)
+        else:
+            attn.kv_append(kt, vt, kc, vc, hkv, d, M, pos)
+            attn.attn_decode(qt, kc, vc, out, hq, hkv, d, M, pos + 1)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        amax, rel = compare(got, ref[t])
+        assert amax <= FP32_ABS and rel <= FP32_REL, (t, amax)
+        tol = FP32_ABS if prec == FP32 else TC_ABS
+        assert np.abs(got - full[pos]).max() <= tol + FP32_ABS
