@@ -449,3 +449,24 @@ def test_autoregressive_steps_match_prefill_rows(attn, prec):
         assert amax <= FP32_ABS and rel <= FP32_REL, (t, amax)
         tol = FP32_ABS if prec == FP32 else TC_ABS
         assert np.abs(got - full[pos]).max() <= tol + FP32_ABS
+
+
+# ------------------------------------------------------------------ bf16 operand mode
+
+BF16 = 2
+
+
+@pytest.mark.parametrize("m,hq,hkv,d", [(300, 4, 2, 128), (129, 2, 1, 64)])
+def test_prefill_bf16_operands(attn, m, hq, hkv, d):
+    """ATTN_PREC_BF16: operands rounded to bf16 (8-bit mantissa, unit roundoff
+    2^-9).  Row 0 alone carries |V| * 2^-9 (about 8e-3 for |V| <= 4.2), and
+    score rounding adds the same order; bound 2.5e-2.  The fp16 mode meets
+    3e-3 on the same inputs."""
+    qs, kvs = hq * d, hkv * d
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, seed=m + d)
+    got = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, BF16)
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs)
+    amax, _ = compare(got, ref)
+    assert amax <= 2.5e-2, amax
+    got16 = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, FP16)
+    assert compare(got16, ref)[0] <= TC_ABS
