@@ -110,6 +110,19 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, TcBarriers*
     atomicExch(&bars->abort, 1u);
 }
 
+// Split-KV scheduling for small grids: a query-tile pair's keys are walked in
+// chunks of kv_chunk tiles by separate CTAs; split pairs leave per-chunk
+// partials that prefill_combine_kernel merges.  kv_chunk = ~0u: no split.
+constexpr uint32_t kNoSplit = 0xffffffffu;
+
+struct SplitArgs {
+    uint32_t kv_chunk;
+    uint32_t n_chunks_max;
+    uint32_t first_split_row;  // rows >= this belong to split pairs
+    float* part_o;             // [heads, m, n_chunks_max, D] unnormalised
+    float* part_ml;            // [heads, m, n_chunks_max, 2] (max in log2 units, sum)
+};
+
 // Number of KV tiles query tile `qt` attends to (0 when the tile is empty).
 __device__ __forceinline__ uint32_t kv_tiles_for(uint32_t qt, uint32_t m) {
     return (qt * kBM < m) ? qt + 1 : 0;  // kBN == kBM: the diagonal tile index is qt
@@ -120,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, uint32_t m,
                   uint32_t num_q_heads, uint32_t heads_per_kv, uint32_t q_stride,
-                  float scale_log2, unsigned int* status, uint64_t wait_ns) {
+                  float scale_log2, unsigned int* status, uint64_t wait_ns,
+                  const SplitArgs split) {
     using L = TcLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -129,16 +143,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
-    const uint32_t pair = n_pairs - 1 - blockIdx.x / num_q_heads;  // heaviest pairs first
     const uint32_t h = blockIdx.x % num_q_heads;
     const uint32_t kvh = h / heads_per_kv;
+    // Work item: (query-tile pair, KV chunk).  Pairs are walked heaviest
+    // first; without a split every pair is one chunk covering all its keys.
+    uint32_t pair = 0, chunk = 0, n_chunks = 1;
+    if (split.kv_chunk == kNoSplit) {
+        pair = n_pairs - 1 - blockIdx.x / num_q_heads;
+    } else {
+        uint32_t idx = blockIdx.x / num_q_heads;
+        for (int p = (int)n_pairs - 1; p >= 0; --p) {
+            const uint32_t nk = max(kv_tiles_for(p * kNQ, m), kv_tiles_for(p * kNQ + 1, m));
+            const uint32_t nc = (nk + split.kv_chunk - 1) / split.kv_chunk;
+            if (idx < nc) {
+                pair = (uint32_t)p;
+                chunk = idx;
+                n_chunks = nc;
+                break;
+            }
+            idx -= nc;
+        }
+    }
     const uint32_t qt0 = pair * kNQ;                                // first query tile index
     uint32_t n_kv[kNQ];
 #pragma unroll
     for (int t = 0; t < kNQ; ++t) n_kv[t] = kv_tiles_for(qt0 + t, m);
-    uint32_t n_kv_all = 0;
+    uint32_t n_kv_pair = 0;
 #pragma unroll
-    for (int t = 0; t < kNQ; ++t) n_kv_all = max(n_kv_all, n_kv[t]);
+    for (int t = 0; t < kNQ; ++t) n_kv_pair = max(n_kv_pair, n_kv[t]);
+    // This item's KV tiles are [j0, j0 + n_it); tile t takes the first tile_n[t]
+    // of them (its causal extent may end inside the chunk).
+    const uint32_t j0 = split.kv_chunk == kNoSplit ? 0u : chunk * split.kv_chunk;
+    const uint32_t n_kv_all =
+        split.kv_chunk == kNoSplit ? n_kv_pair : min(n_kv_pair, j0 + split.kv_chunk) - j0;
+    uint32_t tile_n[kNQ];
+#pragma unroll
+    for (int t = 0; t < kNQ; ++t) tile_n[t] = n_kv[t] > j0 ? min(n_kv[t] - j0, n_kv_all) : 0;
 
     const uint32_t sQ = smem_u32(smem + L::kQOff);
     const uint32_t sK = smem_u32(smem + L::kKOff);
@@ -160,6 +200,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mbar_init(smem_u32(&bars.mma_done), 1);
         bars.abort = 0;
         fence_mbar_init();
+        // A split's combine kernel may launch now; it waits for this grid.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(&bars.tmem_base), kTmemCols);
@@ -193,14 +235,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 for (uint32_t b = 0; b < L::kBoxes; ++b)
                     tma_load_2d(sK + st * L::kKTileBytes + b * (kBN * 128), &tm_k,
                                 smem_u32(&bars.k_full[st]), (int32_t)(kvh * D + b * 64),
-                                (int32_t)(j * kBN));
+                                (int32_t)((j0 + j) * kBN));
                 if (use > 0) ok = mbar_wait(smem_u32(&bars.v_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
                 if (!ok) { issued = j + 1; break; }
                 mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), L::kKTileBytes);
                 for (uint32_t b = 0; b < L::kBoxes; ++b)
                     tma_load_2d(sV + st * L::kKTileBytes + b * (kBN * 128), &tm_v,
                                 smem_u32(&bars.v_full[st]), (int32_t)(kvh * D + b * 64),
-                                (int32_t)(j * kBN));
+                                (int32_t)((j0 + j) * kBN));
                 issued = j + 1;
             }
             if (!ok) record_timeout(status, &bars);
@@ -241,14 +283,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                smem_desc(vb + ks * 2048, kBN * 128, 1024, 2), idesc_pv,
                                (j > 0 || ks > 0) ? 1u : 0u);
                 }
-                if (j + 1 == n_kv[t]) mma_commit(smem_u32(&bars.o_final[t]));
+                if (j + 1 == tile_n[t]) mma_commit(smem_u32(&bars.o_final[t]));
             };
             if (ok && n_kv_all > 0) {
                 ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, wait_ns, status, kStatusTimeout);
                 if (ok) {
                     tc_fence_after();
                     for (int t = 0; t < kNQ; ++t)
-                        if (n_kv[t] > 0) issue_s(t, 0);
+                        if (tile_n[t] > 0) issue_s(t, 0);
                     mma_commit(smem_u32(&bars.k_empty[0]));
                 }
             }
@@ -259,13 +301,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 bool k_next_ready = false;
                 const uint32_t jn = j + 1;
                 for (int t = 0; t < kNQ && ok; ++t) {
-                    if (j < n_kv[t]) {
+                    if (j < tile_n[t]) {
                         ok = mbar_wait(smem_u32(&bars.p_full[t]), j & 1, wait_ns, status, kStatusTimeout);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(t, j);
                     }
-                    if (jn < n_kv[t]) {
+                    if (jn < tile_n[t]) {
                         if (!k_next_ready) {
                             ok = mbar_wait(smem_u32(&bars.k_full[jn % kStages]),
                                            (jn / kStages) & 1, wait_ns, status, kStatusTimeout);
@@ -296,7 +338,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float m_used = -CUDART_INF_F;  // log2 units
         float l_sum = 0.f;
         bool ok = true;
-        const uint32_t nkv = n_kv[t];
+        const uint32_t nkv = tile_n[t];
         for (uint32_t j = 0; j < nkv; ++j) {
             ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, wait_ns, status, kStatusTimeout);
             const bool any_fail = __any_sync(0xffffffffu, !ok);
@@ -309,8 +351,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                 for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
             }
-            if (j + 1 == nkv) {  // diagonal tile: keys above the row are not attended
-                const uint32_t key0 = j * kBN;
+            if (j0 + j + 1 == n_kv[t]) {  // diagonal tile: keys above the row are not attended
+                const uint32_t key0 = (j0 + j) * kBN;
 #pragma unroll
                 for (int c = 0; c < kBN; ++c)
                     if (key0 + c > row) s[c] = -CUDART_INF_F;
@@ -374,7 +416,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (ok && nkv > 0) {
             ok = mbar_wait(smem_u32(&bars.o_final[t]), 0, wait_ns, status, kStatusTimeout);
             if (__any_sync(0xffffffffu, !ok)) ok = false;
-            if (ok) {
+            if (ok && n_chunks > 1) {
+                // One KV chunk of a split pair: unnormalised O and (max, sum)
+                // for the combine kernel.
+                tc_fence_after();
+                const size_t pidx = ((size_t)h * m + row) * split.n_chunks_max + chunk;
+                float* dst = split.part_o + pidx * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32_sync(t_o + c * 32, r);
+                    if (row < m) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + c * 32 + i) =
+                                make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                            __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                    }
+                }
+                if (row < m)
+                    *reinterpret_cast<float2*>(split.part_ml + 2 * pidx) = make_float2(m_used, l_sum);
+            } else if (ok) {
                 tc_fence_after();
                 const float inv_l = 1.0f / l_sum;
                 float* dst = o + (size_t)row * q_stride + (size_t)h * D;
@@ -404,6 +466,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Merge of the KV-chunk partials of split query-tile pairs: one warp per
+// (row, head), lane l holding elements [l*D/32, (l+1)*D/32).  Launched as a
+// programmatic dependent of the prefill kernel.
+template <int D>
+__global__ void __launch_bounds__(256)
+prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
+                       uint32_t num_q_heads, uint32_t q_stride) {
+    constexpr int V = D / 32;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t item = blockIdx.x * 8 + warp;
+    const uint32_t row = split.first_split_row + item / num_q_heads;
+    const uint32_t h = item % num_q_heads;
+    if (row >= m) return;
+    const uint32_t n_kv_tile = row / kBM + 1;  // KV tiles of this row's query tile
+    const uint32_t nct = (n_kv_tile + split.kv_chunk - 1) / split.kv_chunk;
+    const size_t base = ((size_t)h * m + row) * split.n_chunks_max;
+    float M = -CUDART_INF_F;
+    for (uint32_t c = 0; c < nct; ++c) M = fmaxf(M, __ldcg(split.part_ml + 2 * (base + c)));
+    float L = 0.f, O[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) O[e] = 0.f;
+    for (uint32_t c = 0; c < nct; ++c) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(split.part_ml) + base + c);
+        const float f = ex2(ml.x - M);
+        L = fmaf(ml.y, f, L);
+        const float* po = split.part_o + (base + c) * D + lane * V;
+#pragma unroll
+        for (int e = 0; e < V; ++e) O[e] = fmaf(__ldcg(po + e), f, O[e]);
+    }
+    const float inv = 1.0f / L;
+    float* dst = o + (size_t)row * q_stride + (size_t)h * D + lane * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) dst[e] = O[e] * inv;
 }
 
 // fp32 -> fp16/bf16 rounding pre-pass: q [m, q_stride] -> qh [m, hq*d] etc.
@@ -487,18 +585,69 @@ bool encode_operand_map(CUtensorMap* map, const void* base, uint32_t cols, uint3
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+struct PrefillPlan {
+    uint32_t n_items;          // work items per head (pairs, or pair chunks)
+    SplitArgs split;           // kv_chunk == kNoSplit: no split
+    size_t operand_bytes;      // fp16 Q, K, V
+    size_t part_o_bytes, part_ml_bytes;
+};
+
+// Split the KV walk only when the pairs alone leave SMs idle: then take the
+// smallest chunk (most parallelism, shortest item) whose items still fit in
+// one wave.  nk(p) = KV tiles of pair p's second tile.
+PrefillPlan make_plan(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                      int sm_count) {
+    PrefillPlan p{};
+    const uint32_t n_qt = (m + kBM - 1) / kBM;
+    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
+    auto nk = [&](uint32_t pr) { return std::min(kNQ * pr + kNQ, n_qt); };
+    p.n_items = n_pairs;
+    p.split.kv_chunk = kNoSplit;
+    p.split.n_chunks_max = 1;
+    p.split.first_split_row = m;
+    const uint32_t sms = (uint32_t)std::max(sm_count, 1);
+    if (n_pairs > 0 && (uint64_t)n_pairs * num_q_heads < sms) {
+        const uint32_t nk_last = nk(n_pairs - 1);
+        for (uint32_t c = 2; c < nk_last; ++c) {
+            uint32_t items = 0;
+            for (uint32_t pr = 0; pr < n_pairs; ++pr) items += (nk(pr) + c - 1) / c;
+            if ((uint64_t)items * num_q_heads <= sms) {
+                p.n_items = items;
+                p.split.kv_chunk = c;
+                p.split.n_chunks_max = (nk_last + c - 1) / c;
+                uint32_t first = 0;
+                while (first < n_pairs && nk(first) <= c) ++first;
+                p.split.first_split_row = std::min(m, first * kNQ * kBM);
+                break;
+            }
+        }
+    }
+    const size_t qb = (size_t)m * num_q_heads * head_dim * 2;
+    const size_t kb = (size_t)m * num_kv_heads * head_dim * 2;
+    p.operand_bytes = align256(qb) + 2 * align256(kb);
+    if (p.split.kv_chunk != kNoSplit) {
+        p.part_o_bytes = align256((size_t)num_q_heads * m * p.split.n_chunks_max * head_dim * 4);
+        p.part_ml_bytes = align256((size_t)num_q_heads * m * p.split.n_chunks_max * 2 * 4);
+    }
+    return p;
+}
+
 template <int D, bool BF16>
 cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, uint32_t m,
                       uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
                       uint32_t kv_stride, float scale, void* workspace, unsigned int* status,
                       uint64_t wait_ns, cudaStream_t stream) {
     using L = TcLayout<D>;
+    const PrefillPlan plan = make_plan(m, num_q_heads, num_kv_heads, D, device_sm_count());
     const uint32_t q_cols = num_q_heads * D, kv_cols = num_kv_heads * D;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint16_t* qh = reinterpret_cast<uint16_t*>(ws);
     uint16_t* kh = reinterpret_cast<uint16_t*>(ws + align256((size_t)m * q_cols * 2));
     uint16_t* vh = reinterpret_cast<uint16_t*>(
         ws + align256((size_t)m * q_cols * 2) + align256((size_t)m * kv_cols * 2));
+    SplitArgs split = plan.split;
+    split.part_o = reinterpret_cast<float*>(ws + plan.operand_bytes);
+    split.part_ml = reinterpret_cast<float*>(ws + plan.operand_bytes + plan.part_o_bytes);
 
     {
         const size_t work = (size_t)m * q_cols / 8;
@@ -525,20 +674,31 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
-    prefill_tc_kernel<D, BF16><<<n_pairs * num_q_heads, kThreads, L::kSmemAlloc, stream>>>(
+    prefill_tc_kernel<D, BF16><<<plan.n_items * num_q_heads, kThreads, L::kSmemAlloc, stream>>>(
         tq, tk, tv, o, m, num_q_heads, num_q_heads / num_kv_heads, q_stride, scale * kLog2e,
-        status, wait_ns);
-    return cudaGetLastError();
+        status, wait_ns, split);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;
+    const uint32_t rows = m - split.first_split_row;
+    const uint32_t items = rows * num_q_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((items + 7) / 8, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_combine_kernel<D>, split, o, m, num_q_heads, q_stride);
 }
 
 }  // namespace
 
 size_t prefill_tc_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim) {
-    const size_t qb = (size_t)m * num_q_heads * head_dim * 2;
-    const size_t kb = (size_t)m * num_kv_heads * head_dim * 2;
-    return align256(qb) + 2 * align256(kb);
+    const PrefillPlan p = make_plan(m, num_q_heads, num_kv_heads, head_dim, device_sm_count());
+    return p.operand_bytes + p.part_o_bytes + p.part_ml_bytes;
 }
 
 cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, float* o,
