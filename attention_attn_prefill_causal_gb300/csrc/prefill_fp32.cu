@@ -8,12 +8,13 @@
 // end.  Q/O rows use q_stride, K/V rows use kv_stride (packed layout).
 //
 // The page runs one warp per query head, walking all M rows serially and
-// reading K/V through L2.  Here a CTA takes 64 query rows of one head and
-// walks 64-key tiles staged in shared memory, so each K/V row is read from
-// global memory once per 64 query rows instead of once per row:
-//  * a warp owns 8 query rows and works on 4 of them at once, each lane
-//    scoring one key of a 32-key slice (dot product over head_dim from
-//    shared memory: a 128-bit K read per lane, a broadcast Q read);
+// reading K/V through L2.  Here a CTA takes a block of query rows of one
+// head (64 rows, or 16 when the problem is too small to fill the SMs with
+// 64-row blocks) and walks 64-key tiles staged in shared memory, so each K/V
+// row is read from global memory once per block instead of once per row:
+//  * a warp owns 8 (or 2) query rows and works on up to 4 of them at once,
+//    each lane scoring one key of a 32-key slice (dot product over head_dim
+//    from shared memory: a 128-bit K read per lane, a broadcast Q read);
 //  * per row, the slice's max and sum come from warp shuffles; the online
 //    softmax runs in base 2 (scores pre-multiplied by log2 e, as the page
 //    does before ex2);
@@ -30,14 +31,12 @@
 namespace attn {
 namespace {
 
-constexpr int kBM = 64;           // query rows per CTA
 constexpr int kBN = 64;           // keys per tile
 constexpr int kThreads = 256;     // 8 warps
-constexpr int kRowsPerWarp = kBM / (kThreads / 32);
-constexpr int kRowGroup = 4;      // rows a warp scores together
+constexpr int kWarps = kThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+template <int D, int kBM>
 struct Smem {
     static constexpr int kPitch = D + 4;  // pad: 128-bit reads across rows hit distinct banks
     float q[kBM][kPitch];
@@ -73,15 +72,19 @@ __device__ __forceinline__ void load_v_tile(float (*dst)[D], const float* __rest
     }
 }
 
-template <int D>
+// kBM query rows per CTA (64 for large problems; 16 when 64-row blocks
+// would leave most SMs idle, which also shortens each warp's serial chain).
+template <int D, int kBM>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                     const float* __restrict__ v, float* __restrict__ o, uint32_t m,
                     uint32_t heads_per_kv, uint32_t q_stride, uint32_t kv_stride,
                     float scale_log2) {
     constexpr int VEC = D / 32;  // output elements per lane
+    constexpr int kRowsPerWarp = kBM / kWarps;
+    constexpr int kRowGroup = kRowsPerWarp < 4 ? kRowsPerWarp : 4;  // rows scored together
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw);
+    Smem<D, kBM>& sm = *reinterpret_cast<Smem<D, kBM>*>(smem_raw);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t nqb = (m + kBM - 1) / kBM;
@@ -201,24 +204,37 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     }
 }
 
-template <int D>
-cudaError_t launch_d(const float* q, const float* k, const float* v, float* o, uint32_t m,
-                     uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
-                     uint32_t kv_stride, float scale, cudaStream_t stream) {
-    const int smem = (int)sizeof(Smem<D>);
+template <int D, int BM>
+cudaError_t launch_bm(const float* q, const float* k, const float* v, float* o, uint32_t m,
+                      uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
+                      uint32_t kv_stride, float scale, cudaStream_t stream) {
+    const int smem = (int)sizeof(Smem<D, BM>);
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_fp32_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_fp32_kernel<D, BM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid((m + kBM - 1) / kBM, num_q_heads);
-    prefill_fp32_kernel<D><<<grid, kThreads, smem, stream>>>(
+    dim3 grid((m + BM - 1) / BM, num_q_heads);
+    prefill_fp32_kernel<D, BM><<<grid, kThreads, smem, stream>>>(
         q, k, v, o, m, num_q_heads / num_kv_heads, q_stride, kv_stride, scale * kLog2e);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const float* q, const float* k, const float* v, float* o, uint32_t m,
+                     uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
+                     uint32_t kv_stride, float scale, cudaStream_t stream) {
+    // 64-row blocks when they give at least two CTAs per SM, else 16-row blocks.
+    const uint64_t blocks64 = (uint64_t)((m + 63) / 64) * num_q_heads;
+    if (blocks64 >= 2ull * (uint64_t)device_sm_count())
+        return launch_bm<D, 64>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
+                                scale, stream);
+    return launch_bm<D, 16>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride, scale,
+                            stream);
 }
 
 }  // namespace

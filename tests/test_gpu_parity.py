@@ -155,6 +155,13 @@ def test_prefill_fp32_small_head_dims(attn, d):
     _check_prefill(attn, 200, 6, 2, d, FP32, seed=d)
 
 
+@pytest.mark.parametrize("m,hq,hkv", [(1000, 40, 8), (77, 40, 8), (1000, 2, 1)])
+def test_prefill_fp32_both_query_block_sizes(attn, m, hq, hkv):
+    """The fp32 kernel takes 64-row query blocks when they fill the SMs twice
+    over (the first case) and 16-row blocks otherwise; ragged tails in both."""
+    _check_prefill(attn, m, hq, hkv, 64, FP32, seed=m + hq)
+
+
 @pytest.mark.parametrize("prec", [FP16, FP32])
 def test_prefill_padded_strides(attn, prec):
     _check_prefill(attn, 333, 6, 2, 128, prec, seed=7, q_pad=64, kv_pad=128)
