@@ -31,7 +31,7 @@ void set_last_error(const char* msg);
 struct DecodePlan {
     uint32_t window_start;
     uint32_t rows_live;
-    uint32_t heads_per_pass;  // query heads per CTA (1, 2, 4 or 8)
+    uint32_t heads_per_pass;  // query heads per CTA (1, 2, 4, 6 or 8)
     uint32_t n_hgroups;       // query-head groups per KV head
     uint32_t chunk;           // live rows per CTA
     uint32_t rows_per_warp;   // rows per warp: ceil(chunk / warps per CTA)

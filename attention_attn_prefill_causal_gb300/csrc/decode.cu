@@ -14,14 +14,15 @@
 // GB300 design.  The page walks the whole sequence with one 32-lane group
 // per head; a 4096-row cache is then a few microseconds of work for a
 // handful of SMs.  Here one launch covers every SM:
-//  * CTA = (sequence chunk, KV head, group of GP <= 8 query heads), eight
+//  * CTA = (sequence chunk, KV head, group of GP in {1,2,4,6,8} query heads), eight
 //    warps, each warp a contiguous run of rows.  Each K/V row is read from
 //    HBM once for every query head of its GQA group, with 128-bit loads
 //    issued before any arithmetic (lane l holds elements [l*V, l*V+V)).
 //  * A warp takes 4 rows per step, i.e. 4*GP (row, head) dot products.  Each
 //    lane forms its partial sums of all of them, and a reduce-scatter over
-//    the warp (at most 31 shuffles) leaves each lane holding the full score
-//    of one pair.  The online softmax (base 2) then costs one exponential
+//    the warp (at most 31 shuffles) leaves lane j holding the full score of
+//    pair j, ordered head-major (j = 4 * head + row) so that a head's four
+//    rows sit in adjacent lanes.  The online softmax (base 2) then costs one exponential
 //    per lane; the weights reach every lane by shuffle for the P.V update of
 //    the lane's slice of head_dim.  The next step's keys are fetched as soon
 //    as the dot products are formed, its values after the P.V update.
@@ -33,6 +34,10 @@
 //    kernel (its launch overlaps the decode grid; it waits on that grid's
 //    completion in hardware), merges the partials of each query head with a
 //    log-sum-exp and normalises.
+//  * Consecutive calls overlap: each decode launch is a programmatic
+//    dependent of the kernel before it on the stream, and its CTAs prefetch
+//    their K/V rows into L2 while that kernel drains, then wait for it
+//    before reading anything.
 //  * Positions below window_start are never read; their score is -1e4
 //    exactly as on the page, and the final merge adds their weight
 //    exp(-1e4 - max) back.  That weight is zero in fp32 unless every live
@@ -62,7 +67,6 @@ constexpr int kWarps = ATTN_DECODE_WARPS;                 // warps per CTA
 constexpr int kThreads = kWarps * 32;
 constexpr int kWarpsPerSm = ATTN_DECODE_WARPS_PER_SM;     // occupancy the plan aims for
 constexpr int kMinBlocks = kWarpsPerSm / kWarps > 0 ? kWarpsPerSm / kWarps : 1;
-constexpr int kMaxHeadsPerPass = 8;
 constexpr int kRowsPerStep = 4;  // K/V rows a warp holds per step
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaskScore = -1.0e4f;  // the page's replaced score
@@ -92,6 +96,12 @@ struct DecodeArgs {
     uint32_t position;       // appended row, or kNoRow
     float scale_log2;
 };
+
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned start, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -162,6 +172,7 @@ __device__ __forceinline__ void rope_slice(float (&x)[V], const float* cosv, con
 // selected by lane bit o and adds the partner's copy of that half.
 template <int NV>
 __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
+    static_assert(NV >= 4 && NV <= 32 && (NV & (NV - 1)) == 0, "NV must be a power of two");
 #pragma unroll
     for (int o = 16; o >= NV; o >>= 1) {
 #pragma unroll
@@ -204,12 +215,13 @@ template <int D, int GP>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const DecodeArgs a) {
     constexpr int V = D / 32;    // elements of a row per lane
     constexpr int U = kRowsPerStep;
-    constexpr int NV = U * GP;   // (row, head) pairs per warp step
+    constexpr int NV = U * GP;   // (row, head) pairs per warp step, head-major: j = g * U + u
+    constexpr int NR = (NV & (NV - 1)) == 0 ? NV : 32;  // reduced width (a power of two)
     // Scaled (and rotated) queries.  With GP >= 2 they are stored head-pair
     // interleaved, sq[g/2][d][g%2], so one 64-bit read gives element d of two
     // heads for a packed (fp32x2) multiply-add.
     __shared__ __align__(16) float sq[GP * D];
-    __shared__ __align__(16) float2 pbuf[kWarps][32];  // (p, p) per (row, head) pair
+    __shared__ __align__(16) float2 pbuf[kWarps][32];  // (p, p) per pair
     __shared__ __align__(16) float2 cbuf[kWarps][GP];  // (corr, corr) per head
     __shared__ float wm[kWarps][GP], wl[kWarps][GP];
     __shared__ __align__(16) float wo[kWarps][GP][D];
@@ -227,6 +239,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
     const uint32_t r1 = min(r0 + a.rows_per_warp, c1);
     const bool has_new = a.position != kNoRow;
     const size_t kv_base = (size_t)kvh * a.max_seq * D;
+
+    // The launch is a programmatic dependent of the previous kernel on the
+    // stream, so this CTA may start while that kernel drains.  Until the
+    // grid dependency resolves it only warms L2 with its K/V rows (a bulk
+    // prefetch reads memory without using it, and L2 is coherent, so a row
+    // written by the previous kernel is still read fresh below); every read
+    // of data and every write waits for the previous kernel's completion.
+    if (lane == 0 && r1 > r0) {
+        const uint32_t bytes = (r1 - r0) * (uint32_t)D * 4u;
+        bulk_prefetch_l2(a.k_cache + kv_base + (size_t)r0 * D, bytes);
+        bulk_prefetch_l2(a.v_cache + kv_base + (size_t)r0 * D, bytes);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Issue the first step's K/V loads before anything else.
     float kx[U][V], vx[U][V];
@@ -279,10 +304,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
     }
     __syncthreads();
 
-    // Lane l owns the score of pair j = l & (NV - 1) = (u, g) with u = j / GP,
-    // g = j % GP = l % GP; its running max and sum are those of head g.
-    const int my_j = lane & (NV - 1);
-    const int my_u = my_j / GP, my_g = my_j % GP;
+    // Lane l owns the score of pair j = l (head g = j / U, row u = j % U) when
+    // l < NV; the U lanes of a head hold its running max and sum.
+    const int my_u = lane % U, my_g = lane / U;
+    const bool my_live_head = lane < NV && my_g < ng;
     float m_run = -CUDART_INF_F, l_run = 0.f;
     float o[GP][V];
 #pragma unroll
@@ -307,7 +332,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
                 float2 kd[V];  // (k, k): one key element against two heads
 #pragma unroll
                 for (int e = 0; e < V; ++e) kd[e] = make_float2(kx[u][e], kx[u][e]);
-                const bool live = base + u < r1;
 #pragma unroll
                 for (int hp = 0; hp < GP / 2; ++hp) {
                     float2 acc = make_float2(0.f, 0.f);
@@ -316,8 +340,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
 #pragma unroll
                         for (int e = 0; e < V; ++e) acc = __ffma2_rn(qp[e], kd[e], acc);
                     }
-                    part[u * GP + 2 * hp] = live ? acc.x : 0.f;
-                    part[u * GP + 2 * hp + 1] = live ? acc.y : 0.f;
+                    part[(2 * hp) * U + u] = acc.x;
+                    part[(2 * hp + 1) * U + u] = acc.y;
                 }
             }
         } else {
@@ -328,10 +352,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
                 float d = 0.f;
 #pragma unroll
                 for (int e = 0; e < V; ++e) d = fmaf(qv[e], kx[u][e], d);
-                part[u] = (base + u < r1) ? d : 0.f;
+                part[u] = d;
             }
         }
-        float s = reduce_scatter<NV>(part, lane);
+        // GP = 6 gives 24 pairs: reduce them as 32 with zeros in the tail.
+        float red[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) red[i] = i < NV ? part[i] : 0.f;
+        float s = reduce_scatter<NR>(red, lane);
         // The keys of this step are consumed: fetch the next step's keys now.
         const uint32_t nb = base + U;
 #pragma unroll
@@ -340,21 +368,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
                 load_slice_stream<V>(kx[u], a.k_cache + kv_base + (size_t)(nb + u) * D + lane * V);
 
         // ---- online softmax: one exponential per lane
-        if (base + my_u >= r1 || my_g >= ng) s = -CUDART_INF_F;
+        if (base + my_u >= r1 || !my_live_head) s = -CUDART_INF_F;
         float mx = s;
 #pragma unroll
-        for (int off = GP; off < NV; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        for (int off = 1; off < U; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         const float m_new = fmaxf(m_run, mx);
         const bool any = m_new != -CUDART_INF_F;
         const float corr = any ? ex2(m_run - m_new) : 1.f;
         const float p = any ? ex2(s - m_new) : 0.f;
         float psum = p;
 #pragma unroll
-        for (int off = GP; off < NV; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+        for (int off = 1; off < U; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
         l_run = l_run * corr + psum;
         m_run = m_new;
         if (lane < NV) pbuf[warp][lane] = make_float2(p, p);
-        if (lane < GP) cbuf[warp][lane] = make_float2(corr, corr);
+        if (lane < NV && my_u == 0) cbuf[warp][my_g] = make_float2(corr, corr);
         __syncwarp();
 
         // ---- O = O * corr + P V on the lane's slice (packed pairs of elements)
@@ -370,10 +398,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+            for (int g = 0; g < GP; ++g) {
 #pragma unroll
-                for (int g = 0; g < GP; ++g) {
-                    const float2 pd = pbuf[warp][u * GP + g];
+                for (int u = 0; u < U; ++u) {
+                    const float2 pd = pbuf[warp][g * U + u];
 #pragma unroll
                     for (int e = 0; e < V; e += 2) {
                         const float2 r = __ffma2_rn(pd, make_float2(vx[u][e], vx[u][e + 1]),
@@ -389,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
                 const float c = cbuf[warp][g].x;
                 o[g][0] *= c;
 #pragma unroll
-                for (int u = 0; u < U; ++u) o[g][0] = fmaf(pbuf[warp][u * GP + g].x, vx[u][0], o[g][0]);
+                for (int u = 0; u < U; ++u) o[g][0] = fmaf(pbuf[warp][g * U + u].x, vx[u][0], o[g][0]);
             }
         }
         __syncwarp();  // pbuf / cbuf are rewritten by the next step
@@ -401,9 +429,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
     }
 
     // ----------------------------------------------------------- merge the warps
-    if (lane < GP) {
-        wm[warp][lane] = m_run;
-        wl[warp][lane] = l_run;
+    if (lane < NV && my_u == 0) {
+        wm[warp][my_g] = m_run;
+        wl[warp][my_g] = l_run;
     }
 #pragma unroll
     for (int g = 0; g < GP; ++g) store_slice<V>(&wo[warp][g][lane * V], o[g]);
@@ -471,6 +499,9 @@ __global__ void __launch_bounds__(512) decode_combine_kernel(const CombineArgs a
     constexpr int kBatch = 16;  // partials per warp per batch (256 per round trip)
     __shared__ float sm_m[kCW], sm_l[kCW];
     __shared__ float sm_o[kCW][32];
+    // The next call's decode kernel may start now (it only prefetches until
+    // this grid completes).
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t h = blockIdx.x;
@@ -544,8 +575,16 @@ __global__ void kv_append_kernel(const float4* __restrict__ k_src, const float4*
 template <int D, int GP>
 cudaError_t launch_gp(const DecodeArgs& a, const DecodePlan& plan, uint32_t kv_heads,
                       uint32_t num_heads, cudaStream_t stream) {
-    decode_kernel<D, GP><<<dim3(plan.n_splits, kv_heads * plan.n_hgroups), kThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t dcfg = {};
+    dcfg.gridDim = dim3(plan.n_splits, kv_heads * plan.n_hgroups, 1);
+    dcfg.blockDim = dim3(kThreads, 1, 1);
+    dcfg.stream = stream;
+    dcfg.attrs = attr;
+    dcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&dcfg, decode_kernel<D, GP>, a);
     if (e != cudaSuccess || plan.n_splits == 1) return e;
     CombineArgs c{};
     c.part_o = a.part_o;
@@ -562,9 +601,6 @@ cudaError_t launch_gp(const DecodeArgs& a, const DecodePlan& plan, uint32_t kv_h
     cfg.gridDim = dim3(num_heads, D / 32, 1);
     cfg.blockDim = dim3(512, 1, 1);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, c);
@@ -577,6 +613,7 @@ cudaError_t launch_d(const DecodeArgs& a, const DecodePlan& plan, uint32_t kv_he
         case 1: return launch_gp<D, 1>(a, plan, kv_heads, num_heads, stream);
         case 2: return launch_gp<D, 2>(a, plan, kv_heads, num_heads, stream);
         case 4: return launch_gp<D, 4>(a, plan, kv_heads, num_heads, stream);
+        case 6: return launch_gp<D, 6>(a, plan, kv_heads, num_heads, stream);
         default: return launch_gp<D, 8>(a, plan, kv_heads, num_heads, stream);
     }
 }
@@ -589,7 +626,21 @@ DecodePlan make_decode_plan(uint32_t num_heads, uint32_t kv_heads, uint32_t head
     p.window_start = (window > 0 && total_seq > window) ? total_seq - window : 0;
     p.rows_live = total_seq - p.window_start;
     const uint32_t G = kv_heads ? num_heads / kv_heads : 1;
-    p.heads_per_pass = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : kMaxHeadsPerPass));
+    // Query heads per CTA: the width in {1, 2, 4, 6, 8} with the fewest head
+    // groups (each group reads the K/V rows again), then the fewest idle
+    // head slots.
+    p.heads_per_pass = 1;
+    {
+        uint32_t best_groups = ~0u, best_idle = ~0u;
+        for (uint32_t w : {1u, 2u, 4u, 6u, 8u}) {
+            const uint32_t groups = (G + w - 1) / w, idle = groups * w - G;
+            if (groups < best_groups || (groups == best_groups && idle < best_idle)) {
+                best_groups = groups;
+                best_idle = idle;
+                p.heads_per_pass = w;
+            }
+        }
+    }
     p.n_hgroups = (G + p.heads_per_pass - 1) / p.heads_per_pass;
     // kWarpsPerSm / kWarps CTAs on every SM: split the live rows of every KV
     // head group into that many equal chunks (the last warp step of a warp

@@ -239,11 +239,15 @@ def test_decode_lengths(attn, T, d):
     assert amax <= FP32_ABS and rel <= FP32_REL
 
 
-@pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 4), (8, 1), (12, 1), (16, 2), (24, 2), (32, 8)])
-def test_decode_gqa_groups(attn, hq, hkv):
-    """Groups above 8 query heads per KV head take several CTA head-groups."""
-    d, S, T = 128, 2000, 1777
-    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=hq * 7 + hkv)
+@pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 4), (8, 1), (12, 1), (16, 2), (24, 2), (32, 8),
+                                     (6, 2), (10, 2), (6, 1), (14, 2), (20, 2), (36, 3), (40, 4)])
+@pytest.mark.parametrize("d", [32, 128])
+def test_decode_gqa_groups(attn, hq, hkv, d):
+    """Every head-pass width (1, 2, 4, 6, 8 query heads per CTA), idle head
+    slots (groups of 3, 5, 7 and 10), and groups above 8 query heads per KV
+    head, which take several CTA head-groups."""
+    S, T = 2000, 1777
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=hq * 7 + hkv + d)
     got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, T, 0)
     ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, 0)
     amax, rel = compare(got, ref)
@@ -402,6 +406,35 @@ def test_decode_append_equals_unfused_append_then_decode(attn):
     torch.cuda.synchronize()
     assert torch.equal(k1, k2) and torch.equal(v1, v2)
     assert (o1 - o2).abs().max().item() <= 1e-6
+
+
+def test_decode_waits_for_the_kernel_before_it(attn):
+    """Decode launches overlap the previous kernel on the stream (they only
+    prefetch until it completes).  Here the kernels right before each decode
+    rewrite q and the cache row the decode reads: back-to-back calls on one
+    stream must still see the new values."""
+    hq, hkv, d, S, T = 12, 2, 128, 4096, 4096
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=77)
+    q2, kc2, vc2, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=78)
+    dq, dk, dv = q.cuda(), kc.cuda(), vc.cuda()
+    dq2, dk2, dv2 = q2.cuda(), kc2.cuda(), vc2.cuda()
+    outs = [torch.full((hq, d), float("nan"), device="cuda") for _ in range(3)]
+    torch.cuda.synchronize()
+    attn.attn_decode(dq, dk, dv, outs[0], hq, hkv, d, S, T)
+    dq.copy_(dq2)                      # predecessor kernels of the next decode
+    dk[:, T - 1].copy_(dk2[:, T - 1])
+    dv[:, T - 1].copy_(dv2[:, T - 1])
+    attn.attn_decode(dq, dk, dv, outs[1], hq, hkv, d, S, T)
+    attn.attn_decode(dq, dk, dv, outs[2], hq, hkv, d, S, T)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    kh[:, T - 1], vh[:, T - 1] = kc2.numpy()[:, T - 1], vc2.numpy()[:, T - 1]
+    ref0 = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, 0)
+    ref1 = oracle.decode(q2.numpy(), kh, vh, hq, hkv, d, S, T, 0)
+    for got, ref in ((outs[0], ref0), (outs[1], ref1), (outs[2], ref1)):
+        amax, rel = compare(got.cpu().numpy(), ref)
+        assert amax <= FP32_ABS and rel <= FP32_REL
 
 
 def test_decode_workspace_reuse(attn):
