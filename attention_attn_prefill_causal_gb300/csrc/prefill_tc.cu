@@ -31,6 +31,10 @@
 // Rescaling is conditional: the running max used for the exponentials only
 // moves when the row max grows by more than 8 (log2 units); the final O / l
 // is exact either way, and P stays below 2^8.
+// Epilogue: after the CTA's last MMA the K/V ring is free; each softmax
+// thread writes its row of O into 128-byte swizzled staging boxes there, and
+// one thread per tile stores them with TMA tensor stores, so O leaves in
+// whole 128-byte lines rather than one 16-byte piece per row and instruction.
 // Every mbarrier wait is bounded; on a timeout a thread records
 // kStatusTimeout in the device status word, abandons its loop, and the CTA
 // still drains its copies, waits for its MMAs and frees TMEM before exiting.
@@ -74,6 +78,13 @@ struct TcLayout {
     static constexpr uint32_t kVOff = kKOff + kStages * kKTileBytes;
     static constexpr uint32_t kBytes = kVOff + kStages * kKTileBytes;
     static constexpr uint32_t kSmemAlloc = kBytes + 1024;        // room to align to 1 KB
+    // Epilogue: once every MMA has completed, the K/V ring stages the fp32
+    // output tiles for the TMA stores, as D/32 boxes of 128 rows x 128 bytes
+    // (32 floats) in the 128-byte swizzled layout.
+    static constexpr uint32_t kOBoxBytes = kBM * 128;
+    static constexpr uint32_t kOTileBytes = kBM * D * 4;
+    static constexpr uint32_t kStageOff = kKOff;
+    static_assert(kStageOff + kNQ * kOTileBytes <= kBytes, "output staging exceeds the K/V ring");
 };
 
 struct __align__(8) TcBarriers {
@@ -84,7 +95,6 @@ struct __align__(8) TcBarriers {
     uint64_t v_empty[kStages];
     uint64_t s_full[kNQ];
     uint64_t p_full[kNQ];
-    uint64_t o_final[kNQ];
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort;
@@ -119,8 +129,9 @@ struct SplitArgs {
     uint32_t kv_chunk;
     uint32_t n_chunks_max;
     uint32_t first_split_row;  // rows >= this belong to split pairs
-    float* part_o;             // [heads, m, n_chunks_max, D] unnormalised
-    float* part_ml;            // [heads, m, n_chunks_max, 2] (max in log2 units, sum)
+    uint32_t m_pad;            // rows rounded up to whole query tiles
+    float* part_o;             // [n_chunks_max, heads, m_pad, D] unnormalised
+    float* part_ml;            // [n_chunks_max, heads, m_pad, 2] (max in log2 units, sum)
 };
 
 // Number of KV tiles query tile `qt` attends to (0 when the tile is empty).
@@ -131,8 +142,9 @@ __device__ __forceinline__ uint32_t kv_tiles_for(uint32_t qt, uint32_t m) {
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, uint32_t m,
-                  uint32_t num_q_heads, uint32_t heads_per_kv, uint32_t q_stride,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const __grid_constant__ CUtensorMap tm_po, uint32_t m,
+                  uint32_t num_q_heads, uint32_t heads_per_kv,
                   float scale_log2, unsigned int* status, uint64_t wait_ns,
                   const SplitArgs split) {
     using L = TcLayout<D>;
@@ -195,7 +207,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int t = 0; t < kNQ; ++t) {
             mbar_init(smem_u32(&bars.s_full[t]), 1);
             mbar_init(smem_u32(&bars.p_full[t]), kBM);
-            mbar_init(smem_u32(&bars.o_final[t]), 1);
         }
         mbar_init(smem_u32(&bars.mma_done), 1);
         bars.abort = 0;
@@ -283,7 +294,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                smem_desc(vb + ks * 2048, kBN * 128, 1024, 2), idesc_pv,
                                (j > 0 || ks > 0) ? 1u : 0u);
                 }
-                if (j + 1 == tile_n[t]) mma_commit(smem_u32(&bars.o_final[t]));
             };
             if (ok && n_kv_all > 0) {
                 ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, wait_ns, status, kStatusTimeout);
@@ -413,49 +423,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_before();
             mbar_arrive(smem_u32(&bars.p_full[t]));
         }
+        // ---- epilogue.  After the CTA's last MMA the K/V ring is free: each
+        // thread writes its row of O (normalised, or this chunk's unnormalised
+        // partial) into the swizzled staging boxes, and one thread of the
+        // warpgroup stores the tile with TMA (whole 128-byte lines; rows past
+        // m are clipped by the tensor map).
+        const bool split_item = n_chunks > 1;
         if (ok && nkv > 0) {
-            ok = mbar_wait(smem_u32(&bars.o_final[t]), 0, wait_ns, status, kStatusTimeout);
+            ok = mbar_wait(smem_u32(&bars.mma_done), 0, wait_ns, status, kStatusTimeout);
             if (__any_sync(0xffffffffu, !ok)) ok = false;
-            if (ok && n_chunks > 1) {
-                // One KV chunk of a split pair: unnormalised O and (max, sum)
-                // for the combine kernel.
-                tc_fence_after();
-                const size_t pidx = ((size_t)h * m + row) * split.n_chunks_max + chunk;
-                float* dst = split.part_o + pidx * D;
+        }
+        uint8_t* stage = smem + L::kStageOff + t * L::kOTileBytes;
+        if (ok && nkv > 0) {
+            tc_fence_after();
+            const float scale_o = split_item ? 1.f : 1.0f / l_sum;
+            const uint32_t sw = row_in_tile & 7u;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32_sync(t_o + c * 32, r);
-                    if (row < m) {
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32_sync(t_o + c * 32, r);
+                uint8_t* box_row = stage + c * L::kOBoxBytes + row_in_tile * 128;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(dst + c * 32 + i) =
-                                make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                            __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                    }
-                }
-                if (row < m)
-                    *reinterpret_cast<float2*>(split.part_ml + 2 * pidx) = make_float2(m_used, l_sum);
-            } else if (ok) {
-                tc_fence_after();
-                const float inv_l = 1.0f / l_sum;
-                float* dst = o + (size_t)row * q_stride + (size_t)h * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32_sync(t_o + c * 32, r);
-                    if (row < m) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            float4 v4 = make_float4(__uint_as_float(r[i]) * inv_l,
-                                                    __uint_as_float(r[i + 1]) * inv_l,
-                                                    __uint_as_float(r[i + 2]) * inv_l,
-                                                    __uint_as_float(r[i + 3]) * inv_l);
-                            *reinterpret_cast<float4*>(dst + c * 32 + i) = v4;
-                        }
-                    }
+                for (uint32_t q4 = 0; q4 < 8; ++q4) {
+                    const float4 v4 = make_float4(__uint_as_float(r[4 * q4]) * scale_o,
+                                                  __uint_as_float(r[4 * q4 + 1]) * scale_o,
+                                                  __uint_as_float(r[4 * q4 + 2]) * scale_o,
+                                                  __uint_as_float(r[4 * q4 + 3]) * scale_o);
+                    *reinterpret_cast<float4*>(box_row + ((q4 ^ sw) * 16)) = v4;
                 }
             }
+            if (split_item && row < m) {
+                const size_t pidx = ((size_t)chunk * num_q_heads + h) * split.m_pad + row;
+                *reinterpret_cast<float2*>(split.part_ml + 2 * pidx) = make_float2(m_used, l_sum);
+            }
+            fence_proxy_async_smem();
+        }
+        named_barrier(1 + t, 128);
+        if (ok && nkv > 0 && wq == 0 && lane == 0) {
+            const int32_t y0 = (int32_t)((qt0 + t) * kBM);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                const uint32_t src = smem_u32(stage + c * L::kOBoxBytes);
+                if (split_item)
+                    tma_store_2d(&tm_po, src, c * 32,
+                                 (int32_t)((chunk * num_q_heads + h) * split.m_pad) + y0);
+                else
+                    tma_store_2d(&tm_o, src, (int32_t)(h * D + c * 32), y0);
+            }
+            bulk_commit_group();
+            bulk_wait_all();
         }
         if (!ok && lane == 0) record_timeout(status, &bars);
     }
@@ -484,17 +500,20 @@ prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
     if (row >= m) return;
     const uint32_t n_kv_tile = row / kBM + 1;  // KV tiles of this row's query tile
     const uint32_t nct = (n_kv_tile + split.kv_chunk - 1) / split.kv_chunk;
-    const size_t base = ((size_t)h * m + row) * split.n_chunks_max;
+    // partial (c, h, row) sits at index (c * num_q_heads + h) * m_pad + row
+    const size_t base = (size_t)h * split.m_pad + row;
+    const size_t cstride = (size_t)num_q_heads * split.m_pad;
     float M = -CUDART_INF_F;
-    for (uint32_t c = 0; c < nct; ++c) M = fmaxf(M, __ldcg(split.part_ml + 2 * (base + c)));
+    for (uint32_t c = 0; c < nct; ++c)
+        M = fmaxf(M, __ldcg(split.part_ml + 2 * (base + c * cstride)));
     float L = 0.f, O[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) O[e] = 0.f;
     for (uint32_t c = 0; c < nct; ++c) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(split.part_ml) + base + c);
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(split.part_ml) + base + c * cstride);
         const float f = ex2(ml.x - M);
         L = fmaf(ml.y, f, L);
-        const float* po = split.part_o + (base + c) * D + lane * V;
+        const float* po = split.part_o + (base + c * cstride) * D + lane * V;
 #pragma unroll
         for (int e = 0; e < V; ++e) O[e] = fmaf(__ldcg(po + e), f, O[e]);
     }
@@ -583,6 +602,23 @@ bool encode_operand_map(CUtensorMap* map, const void* base, uint32_t cols, uint3
     return r == CUDA_SUCCESS;
 }
 
+// fp32 output map for the epilogue's TMA stores: rows of `cols` floats with a
+// pitch of `row_stride` floats, boxes of 32 floats x box_rows, 128-byte swizzle.
+bool encode_output_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                       uint64_t row_stride, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {row_stride * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gdim,
+                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct PrefillPlan {
@@ -605,6 +641,7 @@ PrefillPlan make_plan(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads, u
     p.split.kv_chunk = kNoSplit;
     p.split.n_chunks_max = 1;
     p.split.first_split_row = m;
+    p.split.m_pad = n_qt * kBM;
     const uint32_t sms = (uint32_t)std::max(sm_count, 1);
     if (n_pairs > 0 && (uint64_t)n_pairs * num_q_heads < sms) {
         const uint32_t nk_last = nk(n_pairs - 1);
@@ -626,8 +663,9 @@ PrefillPlan make_plan(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads, u
     const size_t kb = (size_t)m * num_kv_heads * head_dim * 2;
     p.operand_bytes = align256(qb) + 2 * align256(kb);
     if (p.split.kv_chunk != kNoSplit) {
-        p.part_o_bytes = align256((size_t)num_q_heads * m * p.split.n_chunks_max * head_dim * 4);
-        p.part_ml_bytes = align256((size_t)num_q_heads * m * p.split.n_chunks_max * 2 * 4);
+        const size_t rows = (size_t)p.split.n_chunks_max * num_q_heads * p.split.m_pad;
+        p.part_o_bytes = align256(rows * head_dim * 4);
+        p.part_ml_bytes = align256(rows * 2 * 4);
     }
     return p;
 }
@@ -658,11 +696,19 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to, tpo;
     if (!encode_operand_map(&tq, qh, q_cols, m, kBM, BF16) ||
         !encode_operand_map(&tk, kh, kv_cols, m, kBN, BF16) ||
-        !encode_operand_map(&tv, vh, kv_cols, m, kBN, BF16))
+        !encode_operand_map(&tv, vh, kv_cols, m, kBN, BF16) ||
+        !encode_output_map(&to, o, q_cols, m, q_stride, kBM))
         return cudaErrorNotSupported;
+    if (split.kv_chunk != kNoSplit) {
+        if (!encode_output_map(&tpo, split.part_o, D,
+                               (uint64_t)split.n_chunks_max * num_q_heads * split.m_pad, D, kBM))
+            return cudaErrorNotSupported;
+    } else {
+        tpo = to;  // not used without a split
+    }
 
     static bool attr_set[64] = {};
     int dev = 0;
@@ -675,8 +721,8 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
         attr_set[dev] = true;
     }
     prefill_tc_kernel<D, BF16><<<plan.n_items * num_q_heads, kThreads, L::kSmemAlloc, stream>>>(
-        tq, tk, tv, o, m, num_q_heads, num_q_heads / num_kv_heads, q_stride, scale * kLog2e,
-        status, wait_ns, split);
+        tq, tk, tv, to, tpo, m, num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e, status,
+        wait_ns, split);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;
     const uint32_t rows = m - split.first_split_row;
