@@ -484,17 +484,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
-// Merge of the KV-chunk partials of split query-tile pairs: one warp per
-// (row, head), lane l holding elements [l*D/32, (l+1)*D/32).  Launched as a
-// programmatic dependent of the prefill kernel.
+// Merge of the KV-chunk partials of split query-tile pairs.  A thread owns 8
+// consecutive elements of one (row, head); the 16 (D = 128) threads of a row
+// read and write whole 512-byte rows.  Up to kCombineBatch chunks are merged
+// per round trip: every load of a batch is issued before any is used.
+// Launched as a programmatic dependent of the prefill kernel.
+constexpr uint32_t kCombineBatch = 4;
+
 template <int D>
 __global__ void __launch_bounds__(256)
 prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
                        uint32_t num_q_heads, uint32_t q_stride) {
-    constexpr int V = D / 32;
+    constexpr uint32_t kPerRow = D / 8;  // threads per (row, head)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t item = blockIdx.x * 8 + warp;
+    const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t item = tid / kPerRow, e0 = (tid % kPerRow) * 8;
     const uint32_t row = split.first_split_row + item / num_q_heads;
     const uint32_t h = item % num_q_heads;
     if (row >= m) return;
@@ -503,24 +507,52 @@ prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
     // partial (c, h, row) sits at index (c * num_q_heads + h) * m_pad + row
     const size_t base = (size_t)h * split.m_pad + row;
     const size_t cstride = (size_t)num_q_heads * split.m_pad;
-    float M = -CUDART_INF_F;
-    for (uint32_t c = 0; c < nct; ++c)
-        M = fmaxf(M, __ldcg(split.part_ml + 2 * (base + c * cstride)));
-    float L = 0.f, O[V];
+    float M = -CUDART_INF_F, L = 0.f, O[8];
 #pragma unroll
-    for (int e = 0; e < V; ++e) O[e] = 0.f;
-    for (uint32_t c = 0; c < nct; ++c) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(split.part_ml) + base + c * cstride);
-        const float f = ex2(ml.x - M);
-        L = fmaf(ml.y, f, L);
-        const float* po = split.part_o + (base + c * cstride) * D + lane * V;
+    for (int i = 0; i < 8; ++i) O[i] = 0.f;
+    for (uint32_t c0 = 0; c0 < nct; c0 += kCombineBatch) {
+        float2 ml[kCombineBatch];
+        float4 lo[kCombineBatch], hi[kCombineBatch];
 #pragma unroll
-        for (int e = 0; e < V; ++e) O[e] = fmaf(__ldcg(po + e), f, O[e]);
+        for (uint32_t b = 0; b < kCombineBatch; ++b) {
+            const uint32_t c = c0 + b;
+            if (c < nct) {
+                const size_t pidx = base + c * cstride;
+                ml[b] = __ldcg(reinterpret_cast<const float2*>(split.part_ml) + pidx);
+                const float4* po = reinterpret_cast<const float4*>(split.part_o + pidx * D + e0);
+                lo[b] = __ldcg(po);
+                hi[b] = __ldcg(po + 1);
+            } else {
+                ml[b] = make_float2(-CUDART_INF_F, 0.f);
+                lo[b] = hi[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float Mb = M;
+#pragma unroll
+        for (uint32_t b = 0; b < kCombineBatch; ++b) Mb = fmaxf(Mb, ml[b].x);
+        const float fo = ex2(M - Mb);  // M = -inf on the first batch: 0
+        L *= fo;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) O[i] *= fo;
+#pragma unroll
+        for (uint32_t b = 0; b < kCombineBatch; ++b) {
+            const float f = ex2(ml[b].x - Mb);  // -inf (absent chunk): 0
+            L = fmaf(ml[b].y, f, L);
+            O[0] = fmaf(lo[b].x, f, O[0]);
+            O[1] = fmaf(lo[b].y, f, O[1]);
+            O[2] = fmaf(lo[b].z, f, O[2]);
+            O[3] = fmaf(lo[b].w, f, O[3]);
+            O[4] = fmaf(hi[b].x, f, O[4]);
+            O[5] = fmaf(hi[b].y, f, O[5]);
+            O[6] = fmaf(hi[b].z, f, O[6]);
+            O[7] = fmaf(hi[b].w, f, O[7]);
+        }
+        M = Mb;
     }
     const float inv = 1.0f / L;
-    float* dst = o + (size_t)row * q_stride + (size_t)h * D + lane * V;
-#pragma unroll
-    for (int e = 0; e < V; ++e) dst[e] = O[e] * inv;
+    float4* dst = reinterpret_cast<float4*>(o + (size_t)row * q_stride + (size_t)h * D + e0);
+    dst[0] = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+    dst[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
 }
 
 // fp32 -> fp16/bf16 rounding pre-pass: q [m, q_stride] -> qh [m, hq*d] etc.
@@ -726,9 +758,9 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;
     const uint32_t rows = m - split.first_split_row;
-    const uint32_t items = rows * num_q_heads;
+    const uint64_t threads = (uint64_t)rows * num_q_heads * (D / 8);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((items + 7) / 8, 1, 1);
+    cfg.gridDim = dim3((uint32_t)((threads + 255) / 256), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
