@@ -7,10 +7,12 @@
 // online softmax.  The page does this with one warp per head on CUDA cores;
 // here the two contractions (S = Q K^T and O += P V) run on the tensor core.
 //
-// Precision: a pre-pass rounds Q, K, V (fp32, packed strides) to fp16 with
-// round-to-nearest into a workspace (10-bit mantissa, the same as TF32), the
-// softmax writes P as fp16, and every MMA accumulates in fp32.  Softmax
-// statistics (row max, row sum) and the output stay fp32.
+// Precision: Q, K, V (fp32, packed strides) are rounded to fp16 with
+// round-to-nearest (10-bit mantissa, the same as TF32): K and V by a pre-pass
+// into a workspace, Q inside this kernel (each CTA stages its two fp32 query
+// tiles with TMA and the softmax warps round them once).  The softmax writes
+// P as fp16, and every MMA accumulates in fp32.  Softmax statistics (row max,
+// row sum) and the output stay fp32.
 //
 // CTA work unit: two consecutive 128-row query tiles (A = rows q0..q0+127,
 // B = q0+128..q0+255) of one head; keys are walked in 128-row tiles up to the
@@ -61,6 +63,7 @@ constexpr int kBN = 128;            // keys per KV tile
 constexpr int kNQ = 2;              // query tiles per CTA
 constexpr int kStages = 2;          // K/V ring depth
 constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -85,10 +88,16 @@ struct TcLayout {
     static constexpr uint32_t kOTileBytes = kBM * D * 4;
     static constexpr uint32_t kStageOff = kKOff;
     static_assert(kStageOff + kNQ * kOTileBytes <= kBytes, "output staging exceeds the K/V ring");
+    // Prologue: each fp32 query tile (D/32 boxes of 128 rows x 32 floats,
+    // 128-byte swizzled) is staged in the V ring before V is first loaded.
+    static constexpr uint32_t kQ32Off = kVOff;
+    static constexpr uint32_t kQ32Bytes = kBM * D * 4;
+    static_assert(kQ32Bytes <= kStages * kKTileBytes, "fp32 query tile exceeds the V ring");
 };
 
 struct __align__(8) TcBarriers {
-    uint64_t q_full;
+    uint64_t q_staged[kNQ];   // fp32 Q tile t landed in the staging area
+    uint64_t q_ready[kNQ];    // fp16 Q tile t written (every softmax thread arrives)
     uint64_t k_full[kStages];
     uint64_t k_empty[kStages];
     uint64_t v_full[kStages];
@@ -197,7 +206,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t sV = smem_u32(smem + L::kVOff);
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bars.q_full), 1);
+        for (int t = 0; t < kNQ; ++t) {
+            mbar_init(smem_u32(&bars.q_staged[t]), 1);
+            mbar_init(smem_u32(&bars.q_ready[t]), kSoftmaxThreads);
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&bars.k_full[s]), 1);
             mbar_init(smem_u32(&bars.k_empty[s]), 1);
@@ -229,48 +241,75 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(smem_u32(&bars.q_full), kNQ * L::kQTileBytes);
-            for (int t = 0; t < kNQ; ++t)
-                for (uint32_t b = 0; b < L::kBoxes; ++b)
-                    tma_load_2d(sQ + t * L::kQTileBytes + b * (kBM * 128), &tm_q,
-                                smem_u32(&bars.q_full), (int32_t)(h * D + b * 64),
-                                (int32_t)((qt0 + t) * kBM));
-            bool ok = true;
-            uint32_t issued = 0;
-            for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
+            const uint32_t sQ32 = smem_u32(smem + L::kQ32Off);
+            auto load_q32 = [&](int t) {
+                mbar_arrive_expect_tx(smem_u32(&bars.q_staged[t]), L::kQ32Bytes);
+                for (uint32_t b = 0; b < D / 32; ++b)
+                    tma_load_2d(sQ32 + b * L::kOBoxBytes, &tm_q, smem_u32(&bars.q_staged[t]),
+                                (int32_t)(h * D + b * 32), (int32_t)((qt0 + t) * kBM));
+            };
+            auto load_k = [&](uint32_t j) {
                 const uint32_t st = j % kStages;
-                const uint32_t use = j / kStages;
-                if (use > 0) ok = mbar_wait(smem_u32(&bars.k_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
-                if (!ok) break;
                 mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), L::kKTileBytes);
                 for (uint32_t b = 0; b < L::kBoxes; ++b)
                     tma_load_2d(sK + st * L::kKTileBytes + b * (kBN * 128), &tm_k,
                                 smem_u32(&bars.k_full[st]), (int32_t)(kvh * D + b * 64),
                                 (int32_t)((j0 + j) * kBN));
-                if (use > 0) ok = mbar_wait(smem_u32(&bars.v_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
-                if (!ok) { issued = j + 1; break; }
+            };
+            auto load_v = [&](uint32_t j) {
+                const uint32_t st = j % kStages;
                 mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), L::kKTileBytes);
                 for (uint32_t b = 0; b < L::kBoxes; ++b)
                     tma_load_2d(sV + st * L::kKTileBytes + b * (kBN * 128), &tm_v,
                                 smem_u32(&bars.v_full[st]), (int32_t)(kvh * D + b * 64),
                                 (int32_t)((j0 + j) * kBN));
-                issued = j + 1;
+            };
+            // Q tile 0 and the first K tile, then Q tile 1 once tile 0 has been
+            // converted; V may use its ring only after both.
+            uint32_t q_issued = 0, k_issued = 0, v_issued = 0;
+            load_q32(0);
+            q_issued = 1;
+            if (n_kv_all > 0) {
+                load_k(0);
+                k_issued = 1;
+            }
+            bool ok = mbar_wait(smem_u32(&bars.q_ready[0]), 0, wait_ns, status, kStatusTimeout);
+            if (ok) {
+                load_q32(1);
+                q_issued = 2;
+                ok = mbar_wait(smem_u32(&bars.q_ready[1]), 0, wait_ns, status, kStatusTimeout);
+            }
+            for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
+                const uint32_t st = j % kStages;
+                const uint32_t use = j / kStages;
+                if (j >= k_issued) {
+                    if (use > 0) ok = mbar_wait(smem_u32(&bars.k_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
+                    if (!ok) break;
+                    load_k(j);
+                    k_issued = j + 1;
+                }
+                if (use > 0) ok = mbar_wait(smem_u32(&bars.v_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
+                if (!ok) break;
+                load_v(j);
+                v_issued = j + 1;
             }
             if (!ok) record_timeout(status, &bars);
             // Drain: every copy this CTA issued must land before it exits.
-            mbar_wait(smem_u32(&bars.q_full), 0, kDrainWaitNs);
-            for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j) {
-                const uint32_t st = j % kStages, ph = (j / kStages) & 1;
-                mbar_wait(smem_u32(&bars.k_full[st]), ph, kDrainWaitNs);
-                mbar_wait(smem_u32(&bars.v_full[st]), ph, kDrainWaitNs);
-            }
+            for (uint32_t t = 0; t < q_issued; ++t)
+                mbar_wait(smem_u32(&bars.q_staged[t]), 0, kDrainWaitNs);
+            for (uint32_t j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
+                mbar_wait(smem_u32(&bars.k_full[j % kStages]), (j / kStages) & 1, kDrainWaitNs);
+            for (uint32_t j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
+                mbar_wait(smem_u32(&bars.v_full[j % kStages]), (j / kStages) & 1, kDrainWaitNs);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16(BF16 ? 1u : 0u, 0, 0, kBN, kBM);
             const uint32_t idesc_pv = idesc_f16(BF16 ? 1u : 0u, 0, 1, D, kBM);
-            bool ok = mbar_wait(smem_u32(&bars.q_full), 0, wait_ns, status, kStatusTimeout);
+            bool ok = true;
+            for (int t = 0; t < kNQ && ok; ++t)
+                ok = mbar_wait(smem_u32(&bars.q_ready[t]), 0, wait_ns, status, kStatusTimeout);
             auto issue_s = [&](int t, uint32_t j) {
                 const uint32_t st = j % kStages;
                 const uint32_t qa = sQ + t * L::kQTileBytes, kb = sK + st * L::kKTileBytes;
@@ -345,9 +384,51 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const uint32_t row = (qt0 + t) * kBM + row_in_tile;
         const uint32_t t_s = tmem + t * 256 + ((uint32_t)(wq * 32) << 16);
         const uint32_t t_o = t_s + 128;
+        bool ok = true;
+        // ---- prologue: round the staged fp32 query tiles to fp16/bf16 into
+        // the MMA's 128-byte swizzled K-major layout (all eight warps, one
+        // tile at a time: thread = row wq*32+lane, half the columns per
+        // warpgroup), checking the fp16 range like the pre-pass does for K, V.
+        {
+            const uint32_t qr = row_in_tile;             // row converted by this thread
+            const uint32_t sw = qr & 7u;
+            const uint8_t* q32 = smem + L::kQ32Off;
+            bool overflow = false;
+            for (int tq = 0; tq < kNQ; ++tq) {
+                ok = ok && mbar_wait(smem_u32(&bars.q_staged[tq]), 0, wait_ns, status, kStatusTimeout);
+                if (ok) {
+                    uint8_t* q16 = smem + L::kQOff + tq * L::kQTileBytes;
+#pragma unroll
+                    for (uint32_t c = (uint32_t)t * (D / 16); c < (uint32_t)(t + 1) * (D / 16); ++c) {
+                        // fp16 chunk c = columns 8c..8c+7 = fp32 chunks 2c, 2c+1
+                        const uint32_t k0 = 2 * c, k1 = 2 * c + 1;
+                        const float4 a = *reinterpret_cast<const float4*>(
+                            q32 + (k0 / 8) * L::kOBoxBytes + qr * 128 + (((k0 % 8) ^ sw) * 16));
+                        const float4 b = *reinterpret_cast<const float4*>(
+                            q32 + (k1 / 8) * L::kOBoxBytes + qr * 128 + (((k1 % 8) ^ sw) * 16));
+                        if (!BF16) {
+                            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+                            overflow |= !(mx <= 65504.f);
+                        }
+                        uint4 out;
+                        out.x = pack_half2(a.x, a.y, BF16);
+                        out.y = pack_half2(a.z, a.w, BF16);
+                        out.z = pack_half2(b.x, b.y, BF16);
+                        out.w = pack_half2(b.z, b.w, BF16);
+                        *reinterpret_cast<uint4*>(q16 + (c / 8) * (kBM * 128) + qr * 128 +
+                                                  (((c % 8) ^ sw) * 16)) = out;
+                    }
+                }
+                // Generic-proxy reads and writes of the staging and of the Q
+                // tile are ordered before the next TMA write and the MMAs.
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&bars.q_ready[tq]));
+            }
+            if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicOr(status, kStatusRange);
+        }
         float m_used = -CUDART_INF_F;  // log2 units
         float l_sum = 0.f;
-        bool ok = true;
         const uint32_t nkv = tile_n[t];
         for (uint32_t j = 0; j < nkv; ++j) {
             ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, wait_ns, status, kStatusTimeout);
@@ -555,20 +636,20 @@ prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
     dst[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
 }
 
-// fp32 -> fp16/bf16 rounding pre-pass: q [m, q_stride] -> qh [m, hq*d] etc.
-// grid.y selects the tensor (0 = q, 1 = k, 2 = v).  Each thread converts 8
-// consecutive elements of one row (two 128-bit loads, one 128-bit store).
+// fp32 -> fp16/bf16 rounding pre-pass for the keys and values: k [m,
+// kv_stride] -> kh [m, hkv*d], likewise v (the queries are rounded inside the
+// prefill kernel, each tile once).  grid.y selects the tensor (0 = k, 1 = v).
+// Each thread converts 8 consecutive elements of one row (two 128-bit loads,
+// one 128-bit store).
 template <bool BF16>
-__global__ void round_operands_kernel(const float* __restrict__ q, const float* __restrict__ k,
-                                      const float* __restrict__ v, uint16_t* __restrict__ qh,
+__global__ void round_operands_kernel(const float* __restrict__ k, const float* __restrict__ v,
                                       uint16_t* __restrict__ kh, uint16_t* __restrict__ vh,
-                                      uint32_t m, uint32_t q_cols, uint32_t kv_cols,
-                                      uint32_t q_stride, uint32_t kv_stride,
+                                      uint32_t m, uint32_t kv_cols, uint32_t kv_stride,
                                       unsigned int* status) {
-    const float* src = blockIdx.y == 0 ? q : (blockIdx.y == 1 ? k : v);
-    uint16_t* dst = blockIdx.y == 0 ? qh : (blockIdx.y == 1 ? kh : vh);
-    const uint32_t cols = blockIdx.y == 0 ? q_cols : kv_cols;
-    const uint32_t stride = blockIdx.y == 0 ? q_stride : kv_stride;
+    const float* src = blockIdx.y == 0 ? k : v;
+    uint16_t* dst = blockIdx.y == 0 ? kh : vh;
+    const uint32_t cols = kv_cols;
+    const uint32_t stride = kv_stride;
     const uint32_t per_row = cols / 8;
     const size_t total = (size_t)m * per_row;
     bool overflow = false;
@@ -656,7 +737,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 struct PrefillPlan {
     uint32_t n_items;          // work items per head (pairs, or pair chunks)
     SplitArgs split;           // kv_chunk == kNoSplit: no split
-    size_t operand_bytes;      // fp16 Q, K, V
+    size_t operand_bytes;      // fp16 K, V
     size_t part_o_bytes, part_ml_bytes;
 };
 
@@ -691,9 +772,8 @@ PrefillPlan make_plan(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads, u
             }
         }
     }
-    const size_t qb = (size_t)m * num_q_heads * head_dim * 2;
     const size_t kb = (size_t)m * num_kv_heads * head_dim * 2;
-    p.operand_bytes = align256(qb) + 2 * align256(kb);
+    p.operand_bytes = 2 * align256(kb);
     if (p.split.kv_chunk != kNoSplit) {
         const size_t rows = (size_t)p.split.n_chunks_max * num_q_heads * p.split.m_pad;
         p.part_o_bytes = align256(rows * head_dim * 4);
@@ -711,25 +791,23 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     const PrefillPlan plan = make_plan(m, num_q_heads, num_kv_heads, D, device_sm_count());
     const uint32_t q_cols = num_q_heads * D, kv_cols = num_kv_heads * D;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint16_t* qh = reinterpret_cast<uint16_t*>(ws);
-    uint16_t* kh = reinterpret_cast<uint16_t*>(ws + align256((size_t)m * q_cols * 2));
-    uint16_t* vh = reinterpret_cast<uint16_t*>(
-        ws + align256((size_t)m * q_cols * 2) + align256((size_t)m * kv_cols * 2));
+    uint16_t* kh = reinterpret_cast<uint16_t*>(ws);
+    uint16_t* vh = reinterpret_cast<uint16_t*>(ws + align256((size_t)m * kv_cols * 2));
     SplitArgs split = plan.split;
     split.part_o = reinterpret_cast<float*>(ws + plan.operand_bytes);
     split.part_ml = reinterpret_cast<float*>(ws + plan.operand_bytes + plan.part_o_bytes);
 
     {
-        const size_t work = (size_t)m * q_cols / 8;
+        const size_t work = (size_t)m * kv_cols / 8;
         const uint32_t threads = 256;
         uint32_t blocks = (uint32_t)std::min<size_t>((work + threads - 1) / threads, 4096);
-        round_operands_kernel<BF16><<<dim3(blocks, 3), threads, 0, stream>>>(
-            q, k, v, qh, kh, vh, m, q_cols, kv_cols, q_stride, kv_stride, status);
+        round_operands_kernel<BF16><<<dim3(blocks, 2), threads, 0, stream>>>(
+            k, v, kh, vh, m, kv_cols, kv_stride, status);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tq, tk, tv, to, tpo;
-    if (!encode_operand_map(&tq, qh, q_cols, m, kBM, BF16) ||
+    if (!encode_output_map(&tq, q, q_cols, m, q_stride, kBM) ||
         !encode_operand_map(&tk, kh, kv_cols, m, kBN, BF16) ||
         !encode_operand_map(&tv, vh, kv_cols, m, kBN, BF16) ||
         !encode_output_map(&to, o, q_cols, m, q_stride, kBM))

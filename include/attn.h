@@ -44,9 +44,11 @@ typedef enum {
      * {32, 64, 128}). */
     ATTN_PREC_FP32 = 0,
     /* Tensor-core mode: Q, K, V rounded to fp16 (round-to-nearest, 10-bit
-     * mantissa as in TF32) in a pre-pass, P rounded to fp16, tcgen05 MMAs
-     * with fp32 accumulation, fp32 softmax statistics and fp32 output.
-     * head_dim in {64, 128}; |q|, |k|, |v| must stay below 65504. */
+     * mantissa as in TF32; K and V by a pre-pass into the workspace, Q
+     * inside the kernel), P rounded to fp16, tcgen05 MMAs with fp32
+     * accumulation, fp32 softmax statistics and fp32 output.  head_dim in
+     * {64, 128}; |q|, |k|, |v| must stay below 65504 (a larger input sets
+     * ATTN_ERR_RANGE in the device status). */
     ATTN_PREC_FP16 = 1,
     /* As ATTN_PREC_FP16 with bf16 operands (8-bit mantissa): wider range,
      * larger rounding error. */
@@ -86,7 +88,9 @@ attn_status_t attn_prefill_causal(const float* q, const float* k, const float* v
                                   size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace attn_prefill_causal needs for these sizes
- * (0 for ATTN_PREC_FP32).  Pure function of its arguments. */
+ * (0 for ATTN_PREC_FP32): the fp16 K and V, plus per-chunk partials when
+ * the call splits its key walk (small problems).  Depends only on the
+ * arguments and on the current device's SM count. */
 size_t attn_prefill_workspace_size(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                    uint32_t head_dim, int precision);
 

@@ -59,7 +59,7 @@ def test_status_strings(attn):
 def test_workspace_sizes_are_pure_functions(attn):
     assert attn.attn_prefill_workspace_size(2048, 12, 2, 128, attn.ATTN_PREC_FP32) == 0
     ws = attn.attn_prefill_workspace_size(2048, 12, 2, 128, attn.ATTN_PREC_FP16)
-    assert ws >= 2048 * 128 * (12 + 4) * 2
+    assert ws >= 2 * 2048 * (2 * 128) * 2       # fp16 K and V
     assert ws == attn.attn_prefill_workspace_size(2048, 12, 2, 128, attn.ATTN_PREC_FP16)
     d = attn.attn_decode_workspace_size(12, 2, 128, 4096, 0)
     assert d > 12 * 128 * 4
