@@ -162,6 +162,17 @@ def test_prefill_fp32_both_query_block_sizes(attn, m, hq, hkv):
     _check_prefill(attn, m, hq, hkv, 64, FP32, seed=m + hq)
 
 
+def test_prefill_split_into_many_key_chunks(attn):
+    """4096 tokens over 2 query heads leave most SMs idle, so the key walk of
+    each query-tile pair is split into 4-tile chunks: up to 8 chunk partials
+    per row, more than one batch of the combine.  Sampled rows include the
+    first and last tiles."""
+    m, hq, hkv, d = 4096, 2, 1, 64
+    rows = workloads.sample_rows(m, 91)
+    amax, _ = _check_prefill(attn, m, hq, hkv, d, FP16, seed=91, rows=rows)
+    print(f"split prefill m={m}: {len(rows)} rows, max abs {amax:.3e}")
+
+
 @pytest.mark.parametrize("prec", [FP16, FP32])
 def test_prefill_padded_strides(attn, prec):
     _check_prefill(attn, 333, 6, 2, 128, prec, seed=7, q_pad=64, kv_pad=128)
