@@ -225,14 +225,17 @@ def test_prefill_rows_beyond_m_untouched(attn):
         assert torch.isfinite(o[: m * qs]).all().item()
 
 
-def test_prefill_tensor_path_rejects_fp16_overflow(attn):
-    """An input beyond the fp16 range is flagged (ATTN_ERR_RANGE) by the
-    rounding pre-pass instead of silently producing inf."""
-    m, hq, hkv, d = 64, 1, 1, 64
-    q, k, v = workloads.prefill_inputs(m, d, d, 4)
-    k[5, 3] = 1.0e5
-    buf, o = guarded_empty(m * d)
-    attn.attn_prefill_causal(q.cuda(), k.cuda(), v.cuda(), o, m, hq, hkv, d, d, d, precision=FP16)
+@pytest.mark.parametrize("where", ["q", "k", "v"])
+def test_prefill_tensor_path_rejects_fp16_overflow(attn, where):
+    """An input beyond the fp16 range is flagged (ATTN_ERR_RANGE) instead of
+    silently producing inf: K and V by the rounding pre-pass, Q by the
+    prefill kernel's own rounding of its query tiles."""
+    m, hq, hkv, d = 300, 2, 1, 64
+    q, k, v = workloads.prefill_inputs(m, hq * d, hkv * d, 4)
+    {"q": q, "k": k, "v": v}[where][257, 3] = -1.0e5   # inside the second query-tile pair
+    buf, o = guarded_empty(m * hq * d)
+    attn.attn_prefill_causal(q.cuda(), k.cuda(), v.cuda(), o, m, hq, hkv, d, hq * d, hkv * d,
+                             precision=FP16)
     assert attn.attn_get_device_status() == attn.ATTN_ERR_RANGE
     assert attn.attn_get_device_status() == attn.ATTN_OK  # cleared by the read
 
