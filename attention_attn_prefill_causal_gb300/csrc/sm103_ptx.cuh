@@ -108,8 +108,16 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Order this thread's earlier global-memory accesses (generic proxy) with
+// its later async-proxy (TMA) accesses of global memory, and vice versa.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // Barrier over `count` threads (a multiple of 32) on hardware barrier `id`.
+// Every lane of each participating warp calls it; the warp reconverges
+// first (bar.sync is warp-aligned).
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+    __syncwarp();
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
