@@ -88,11 +88,12 @@ struct TcLayout {
     static constexpr uint32_t kOTileBytes = kBM * D * 4;
     static constexpr uint32_t kStageOff = kKOff;
     static_assert(kStageOff + kNQ * kOTileBytes <= kBytes, "output staging exceeds the K/V ring");
-    // Prologue: each fp32 query tile (D/32 boxes of 128 rows x 32 floats,
-    // 128-byte swizzled) is staged in the V ring before V is first loaded.
-    static constexpr uint32_t kQ32Off = kVOff;
+    // Prologue: the two fp32 query tiles (D/32 boxes of 128 rows x 32 floats,
+    // 128-byte swizzled) are staged at once, tile 0 in the K ring and tile 1
+    // in the V ring, before K and V are first loaded.
     static constexpr uint32_t kQ32Bytes = kBM * D * 4;
-    static_assert(kQ32Bytes <= kStages * kKTileBytes, "fp32 query tile exceeds the V ring");
+    __host__ __device__ static constexpr uint32_t q32_off(int t) { return t == 0 ? kKOff : kVOff; }
+    static_assert(kQ32Bytes <= kStages * kKTileBytes, "fp32 query tile exceeds a K/V ring");
 };
 
 struct __align__(8) TcBarriers {
@@ -241,11 +242,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            const uint32_t sQ32 = smem_u32(smem + L::kQ32Off);
             auto load_q32 = [&](int t) {
+                const uint32_t dst = smem_u32(smem + L::q32_off(t));
                 mbar_arrive_expect_tx(smem_u32(&bars.q_staged[t]), L::kQ32Bytes);
                 for (uint32_t b = 0; b < D / 32; ++b)
-                    tma_load_2d(sQ32 + b * L::kOBoxBytes, &tm_q, smem_u32(&bars.q_staged[t]),
+                    tma_load_2d(dst + b * L::kOBoxBytes, &tm_q, smem_u32(&bars.q_staged[t]),
                                 (int32_t)(h * D + b * 32), (int32_t)((qt0 + t) * kBM));
             };
             auto load_k = [&](uint32_t j) {
@@ -264,21 +265,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                 smem_u32(&bars.v_full[st]), (int32_t)(kvh * D + b * 64),
                                 (int32_t)((j0 + j) * kBN));
             };
-            // Q tile 0 and the first K tile, then Q tile 1 once tile 0 has been
-            // converted; V may use its ring only after both.
+            // Both query tiles at once; the first K tile as soon as tile 0
+            // (staged in the K ring) is converted, V after tile 1.
             uint32_t q_issued = 0, k_issued = 0, v_issued = 0;
             load_q32(0);
-            q_issued = 1;
-            if (n_kv_all > 0) {
+            load_q32(1);
+            q_issued = 2;
+            bool ok = mbar_wait(smem_u32(&bars.q_ready[0]), 0, wait_ns, status, kStatusTimeout);
+            if (ok && n_kv_all > 0) {
                 load_k(0);
                 k_issued = 1;
             }
-            bool ok = mbar_wait(smem_u32(&bars.q_ready[0]), 0, wait_ns, status, kStatusTimeout);
-            if (ok) {
-                load_q32(1);
-                q_issued = 2;
-                ok = mbar_wait(smem_u32(&bars.q_ready[1]), 0, wait_ns, status, kStatusTimeout);
-            }
+            if (ok) ok = mbar_wait(smem_u32(&bars.q_ready[1]), 0, wait_ns, status, kStatusTimeout);
             for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
                 const uint32_t st = j % kStages;
                 const uint32_t use = j / kStages;
@@ -387,16 +385,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         bool ok = true;
         // ---- prologue: round the staged fp32 query tiles to fp16/bf16 into
         // the MMA's 128-byte swizzled K-major layout (all eight warps, one
-        // tile at a time: thread = row wq*32+lane, half the columns per
+        // tile after the other: thread = row wq*32+lane, half the columns per
         // warpgroup), checking the fp16 range like the pre-pass does for K, V.
         {
             const uint32_t qr = row_in_tile;             // row converted by this thread
             const uint32_t sw = qr & 7u;
-            const uint8_t* q32 = smem + L::kQ32Off;
+
             bool overflow = false;
             for (int tq = 0; tq < kNQ; ++tq) {
                 ok = ok && mbar_wait(smem_u32(&bars.q_staged[tq]), 0, wait_ns, status, kStatusTimeout);
                 if (ok) {
+                    const uint8_t* q32 = smem + L::q32_off(tq);
                     uint8_t* q16 = smem + L::kQOff + tq * L::kQTileBytes;
 #pragma unroll
                     for (uint32_t c = (uint32_t)t * (D / 16); c < (uint32_t)(t + 1) * (D / 16); ++c) {
@@ -519,17 +518,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             const float scale_o = split_item ? 1.f : 1.0f / l_sum;
             const uint32_t sw = row_in_tile & 7u;
+            // the whole row of O in one TMEM load (one wait)
+            uint32_t r[D];
+            if constexpr (D == 128) {
+                tmem_ld128_sync(t_o, r);
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c)
+                    tmem_ld32(t_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+                tmem_wait_ld();
+            }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32_sync(t_o + c * 32, r);
                 uint8_t* box_row = stage + c * L::kOBoxBytes + row_in_tile * 128;
 #pragma unroll
                 for (uint32_t q4 = 0; q4 < 8; ++q4) {
-                    const float4 v4 = make_float4(__uint_as_float(r[4 * q4]) * scale_o,
-                                                  __uint_as_float(r[4 * q4 + 1]) * scale_o,
-                                                  __uint_as_float(r[4 * q4 + 2]) * scale_o,
-                                                  __uint_as_float(r[4 * q4 + 3]) * scale_o);
+                    const uint32_t i = c * 32 + 4 * q4;
+                    const float4 v4 = make_float4(__uint_as_float(r[i]) * scale_o,
+                                                  __uint_as_float(r[i + 1]) * scale_o,
+                                                  __uint_as_float(r[i + 2]) * scale_o,
+                                                  __uint_as_float(r[i + 3]) * scale_o);
                     *reinterpret_cast<float4*>(box_row + ((q4 ^ sw) * 16)) = v4;
                 }
             }
@@ -552,7 +560,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     tma_store_2d(&tm_o, src, (int32_t)(h * D + c * 32), y0);
             }
             bulk_commit_group();
-            bulk_wait_all();
+            bulk_wait_all_read();  // the staging must outlive the reads, not the writes
         }
         if (!ok && lane == 0) record_timeout(status, &bars);
     }

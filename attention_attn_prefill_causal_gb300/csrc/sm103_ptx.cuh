@@ -103,6 +103,12 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Wait until every committed bulk group of this thread has finished reading
+// its shared-memory source (the global writes may still be in flight; they
+// complete before the grid does).
+__device__ __forceinline__ void bulk_wait_all_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
