@@ -1,6 +1,7 @@
 // attn_internal.h -- host-side declarations shared by the library's
 // translation units (not part of the public C ABI).
 #pragma once
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -26,6 +27,22 @@ attn_status_t record_cuda_error(cudaError_t err);
 
 // Set the text attn_last_error_string() returns on this host thread.
 void set_last_error(const char* msg);
+
+// Raise Kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (any host thread may call it; devices past the
+// cached range set it on every call).
+template <auto Kernel>
+cudaError_t ensure_dynamic_smem(int bytes) {
+    static std::atomic<bool> done[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < 64;
+    if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && cached) done[dev].store(true, std::memory_order_release);
+    return e;
+}
 
 // ---------------------------------------------------------------- decode
 struct DecodePlan {

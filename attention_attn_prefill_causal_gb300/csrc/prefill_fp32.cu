@@ -209,15 +209,8 @@ cudaError_t launch_bm(const float* q, const float* k, const float* v, float* o, 
                       uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
                       uint32_t kv_stride, float scale, cudaStream_t stream) {
     const int smem = (int)sizeof(Smem<D, BM>);
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_fp32_kernel<D, BM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
+    const cudaError_t e = ensure_dynamic_smem<prefill_fp32_kernel<D, BM>>(smem);
+    if (e != cudaSuccess) return e;
     dim3 grid((m + BM - 1) / BM, num_q_heads);
     prefill_fp32_kernel<D, BM><<<grid, kThreads, smem, stream>>>(
         q, k, v, o, m, num_q_heads / num_kv_heads, q_stride, kv_stride, scale * kLog2e);

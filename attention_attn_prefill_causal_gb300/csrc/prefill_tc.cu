@@ -828,15 +828,9 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
         tpo = to;  // not used without a split
     }
 
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, BF16>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)L::kSmemAlloc);
+    {
+        const cudaError_t e = ensure_dynamic_smem<prefill_tc_kernel<D, BF16>>((int)L::kSmemAlloc);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
     }
     prefill_tc_kernel<D, BF16><<<plan.n_items * num_q_heads, kThreads, L::kSmemAlloc, stream>>>(
         tq, tk, tv, to, tpo, m, num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e, status,
