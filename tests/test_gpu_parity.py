@@ -162,6 +162,15 @@ def test_prefill_fp32_both_query_block_sizes(attn, m, hq, hkv):
     _check_prefill(attn, m, hq, hkv, 64, FP32, seed=m + hq)
 
 
+def test_prefill_long_sequence_sampled_rows(attn):
+    """32768 tokens over 2 query heads: query tiles walk up to 256 key tiles,
+    and the 256 CTAs take more than one wave on the SMs."""
+    m, hq, hkv, d = 32768, 2, 1, 128
+    rows = workloads.sample_rows(m, 321, n_random=128)
+    amax, _ = _check_prefill(attn, m, hq, hkv, d, FP16, seed=321, rows=rows)
+    print(f"prefill m={m}: {len(rows)} rows, max abs {amax:.3e}")
+
+
 def test_prefill_split_into_many_key_chunks(attn):
     """4096 tokens over 2 query heads leave most SMs idle, so the key walk of
     each query-tile pair is split into 4-tile chunks: up to 8 chunk partials
@@ -266,6 +275,18 @@ def test_decode_gqa_groups(attn, hq, hkv, d):
     ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, T, 0)
     amax, rel = compare(got, ref)
     assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+@pytest.mark.parametrize("W", [0, 8191])
+def test_decode_long_cache(attn, W):
+    """131072 cached rows: each warp walks about 27 four-row steps (W = 0),
+    or a window ending at the last row that starts inside a chunk."""
+    hq, hkv, d, S = 12, 2, 128, 131072
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=131)
+    got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, S, W)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, S, W)
+    amax, rel = compare(got, ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
 
 
 @pytest.mark.parametrize("T,W", [(4096, 1), (4096, 7), (4096, 4095), (4096, 4096), (4096, 5000),
