@@ -14,18 +14,20 @@
 // GB300 design.  The page walks the whole sequence with one 32-lane group
 // per head; a 4096-row cache is then a few microseconds of work for a
 // handful of SMs.  Here one launch covers every SM:
-//  * CTA = (sequence chunk, KV head, group of GP in {1,2,4,6,8} query heads), eight
-//    warps, each warp a contiguous run of rows.  Each K/V row is read from
-//    HBM once for every query head of its GQA group, with 128-bit loads
-//    issued before any arithmetic (lane l holds elements [l*V, l*V+V)).
+//  * CTA = (sequence chunk, KV head, group of GP in {1,2,4,6,8} query
+//    heads), eight warps, each warp a contiguous run of rows.  Each K/V row
+//    is read from HBM once for every query head of its GQA group, with
+//    128-bit loads issued before any arithmetic (lane l holds elements
+//    [l*V, l*V+V)).
 //  * A warp takes 4 rows per step, i.e. 4*GP (row, head) dot products.  Each
 //    lane forms its partial sums of all of them, and a reduce-scatter over
 //    the warp (at most 31 shuffles) leaves lane j holding the full score of
 //    pair j, ordered head-major (j = 4 * head + row) so that a head's four
-//    rows sit in adjacent lanes.  The online softmax (base 2) then costs one exponential
-//    per lane; the weights reach every lane by shuffle for the P.V update of
-//    the lane's slice of head_dim.  The next step's keys are fetched as soon
-//    as the dot products are formed, its values after the P.V update.
+//    rows sit in adjacent lanes.  The online softmax (base 2) then costs one
+//    exponential per lane; the weights reach every lane through shared
+//    memory, as (p, p) pairs for the packed P.V update of the lane's slice of
+//    head_dim.  The next step's keys are fetched as soon as the dot products
+//    are formed, its values after the P.V update.
 //  * The warps' states merge in shared memory and each CTA writes one
 //    partial (max, sum, unnormalised output) per query head to the
 //    workspace; with a single chunk per KV head the CTA writes the

@@ -19,7 +19,9 @@
 // diagonal.  Warp roles (320 threads):
 //   warps 0-3  softmax for tile A  (thread r owns TMEM lane r = query row r)
 //   warps 4-7  softmax for tile B
-//   warp  8    TMA producer: Q tiles once, then K and V tiles into a
+//   warp  8    TMA producer: both fp32 Q tiles once (staged in the K and
+//              V rings, which the softmax warps then free by rounding them
+//              into the fp16 Q tiles), then K and V tiles into a
 //              two-stage ring
 //   warp  9    TMEM allocator and MMA issuer (one thread)
 // TMEM (512 columns): per tile, S/P in 128 columns (P is written as packed
