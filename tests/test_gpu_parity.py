@@ -264,7 +264,7 @@ def test_decode_lengths(attn, T, d):
 
 @pytest.mark.parametrize("hq,hkv", [(1, 1), (4, 4), (8, 1), (12, 1), (16, 2), (24, 2), (32, 8),
                                      (6, 2), (10, 2), (6, 1), (14, 2), (20, 2), (36, 3), (40, 4)])
-@pytest.mark.parametrize("d", [32, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 def test_decode_gqa_groups(attn, hq, hkv, d):
     """Every head-pass width (1, 2, 4, 6, 8 query heads per CTA), idle head
     slots (groups of 3, 5, 7 and 10), and groups above 8 query heads per KV
