@@ -101,13 +101,14 @@ def _check(status: int, where: str, check: bool) -> int:
 
 
 def _workspace(nbytes: int, like, workspace):
-    """A zeroed device workspace (the decode workspace starts with arrival
-    counters that must be zero before its first use)."""
+    """The caller's workspace, or a new device buffer of nbytes.  Neither
+    entry point reads workspace bytes it has not written in the same call,
+    so the buffer is left uninitialised."""
     if workspace is not None or nbytes == 0:
         return workspace
     import torch
     dev = like.device if hasattr(like, "device") else torch.device("cuda", torch.cuda.current_device())
-    return torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    return torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
 
 def attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim, precision=ATTN_PREC_FP16):
