@@ -171,6 +171,34 @@ def test_prefill_long_sequence_sampled_rows(attn):
     print(f"prefill m={m}: {len(rows)} rows, max abs {amax:.3e}")
 
 
+@pytest.mark.parametrize("prec", [FP16, FP32])
+def test_prefill_sharp_softmax(attn, prec):
+    """scale 2 on N(0,1) inputs (head_dim 128): scores spread over about
+    +-100 in log2 units, so the running max moves past the rescale threshold
+    many times and the O rescale path runs often."""
+    m, hq, hkv, d = 700, 4, 2, 128
+    qs, kvs = hq * d, hkv * d
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, 77)
+    got = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, prec, scale=2.0)
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs, scale=2.0)
+    amax, rel = compare(got, ref)
+    if prec == FP32:
+        assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
+    else:
+        # fp16 operand rounding perturbs a score by about scale*|q||k|*2^-11,
+        # so the bound of the default scale 1/sqrt(d) grows by scale*sqrt(d).
+        assert amax <= TC_ABS * 2.0 * math.sqrt(d), amax
+
+
+def test_decode_sharp_softmax(attn):
+    hq, hkv, d, S = 12, 2, 128, 4096
+    q, kc, vc, _, _ = workloads.decode_inputs(hq, hkv, d, S, seed=78)
+    got = _run_decode(attn, q, kc, vc, hq, hkv, d, S, S, 0, scale=2.0)
+    ref = oracle.decode(q.numpy(), kc.numpy(), vc.numpy(), hq, hkv, d, S, S, 0, scale=2.0)
+    amax, rel = compare(got, ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
+
+
 def test_prefill_split_into_many_key_chunks(attn):
     """4096 tokens over 2 query heads leave most SMs idle, so the key walk of
     each query-tile pair is split into 4-tile chunks: up to 8 chunk partials

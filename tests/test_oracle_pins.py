@@ -161,6 +161,32 @@ def test_scale_zero_gives_mean_of_values():
             np.testing.assert_allclose(out[i, h], v64[:i + 1].mean(0), rtol=0, atol=1e-13)
 
 
+def test_huge_scale_gives_the_argmax_value_row():
+    """With a very large scale the softmax becomes an argmax: each output is
+    the V row of the key with the highest score (unique for random inputs).
+    Scores reach about 1e5 here, so an oracle that exponentiates without
+    subtracting the row max overflows; a scale applied in the wrong place
+    picks the wrong row."""
+    m, hq, hkv, d = 9, 2, 1, 32
+    q, k, v, qs, kvs = _packed(m, hq, hkv, d, 57)
+    big = 2.0e4
+    out = oracle.prefill_causal(q, k, v, m, hq, hkv, d, qs, kvs, scale=big)
+    q64, k64, v64 = (x.astype(np.float64) for x in (q, k, v))
+    for i in range(m):
+        for h in range(hq):
+            s = k64[:i + 1, :d] @ q64[i, h * d:(h + 1) * d]
+            order = np.sort(s)
+            if i > 0:
+                assert big * (order[-1] - order[-2]) > 50  # the argmax is decisive
+            np.testing.assert_allclose(out[i, h], v64[int(np.argmax(s)), :d], rtol=0, atol=1e-12)
+    S = 16
+    qd, kc, vc = _rand((hq, d), 58), _rand((hkv, S, d), 59), _rand((hkv, S, d), 60)
+    outd = oracle.decode(qd, kc, vc, hq, hkv, d, S, S, 0, scale=big)
+    for h in range(hq):
+        s = kc[0].astype(np.float64) @ qd[h].astype(np.float64)
+        np.testing.assert_allclose(outd[h], vc[0, int(np.argmax(s))], rtol=0, atol=1e-12)
+
+
 def test_key_shift_invariance():
     """Adding one vector c to every key adds scale*q.c to every score of a query,
     which softmax cancels (shift invariance)."""
