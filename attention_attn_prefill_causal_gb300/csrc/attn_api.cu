@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "attn_internal.h"
@@ -54,10 +55,15 @@ unsigned int* device_status_ptr() {
 }
 
 int device_sm_count() {
+    static std::atomic<int> cached[64];  // 0 = not queried yet
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-        return n;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        if (dev >= 0 && dev < 64 && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+            if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
+            return n;
+        }
+    }
     cudaGetLastError();  // no device visible: clear the sticky query error
     return 152;
 }
