@@ -12,14 +12,17 @@
 // head (64 rows, or 16 when the problem is too small to fill the SMs with
 // 64-row blocks) and walks 64-key tiles staged in shared memory, so each K/V
 // row is read from global memory once per block instead of once per row:
-//  * a warp owns 8 (or 2) query rows and works on up to 4 of them at once,
-//    each lane scoring one key of a 32-key slice (dot product over head_dim
-//    from shared memory: a 128-bit K read per lane, a broadcast Q read);
-//  * per row, the slice's max and sum come from warp shuffles; the online
+//  * a warp owns 8 (or 2) query rows and scores all of them at once, each
+//    lane taking keys lane and lane + 32 of the tile (dot products over
+//    head_dim from shared memory: two 128-bit K reads per lane feed every
+//    row, the Q reads are broadcasts), so each shared-memory wavefront
+//    feeds about 128 FMAs;
+//  * per row, the tile's max and sum come from warp shuffles; the online
 //    softmax runs in base 2 (scores pre-multiplied by log2 e, as the page
 //    does before ex2);
 //  * for PV each lane owns head_dim/32 output elements and takes the
-//    slice's weights by shuffle.
+//    weights by shuffle, one 32-key half at a time (a half entirely above
+//    the warp's rows is skipped).
 // Causal masking is the loop bound plus a per-key test on the diagonal tile.
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -82,7 +85,6 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                     float scale_log2) {
     constexpr int VEC = D / 32;  // output elements per lane
     constexpr int kRowsPerWarp = kBM / kWarps;
-    constexpr int kRowGroup = kRowsPerWarp < 4 ? kRowsPerWarp : 4;  // rows scored together
     extern __shared__ __align__(16) uint8_t smem_raw[];
     Smem<D, kBM>& sm = *reinterpret_cast<Smem<D, kBM>*>(smem_raw);
 
@@ -104,6 +106,7 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
         for (int e = 0; e < VEC; ++e) acc[r][e] = 0.f;
     }
     const int wr0 = warp * kRowsPerWarp;        // first local row of this warp
+    const uint32_t wrow_last = q0 + wr0 + kRowsPerWarp - 1;
     const uint32_t last_row = min(q0 + kBM, m) - 1;
     const uint32_t n_tiles = last_row / kBN + 1;
 
@@ -113,75 +116,81 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
         load_tile<D>(sm.k, k, k0, m, kv_stride, kvh * D, kBN);
         load_v_tile<D>(sm.v, v, k0, m, kv_stride, kvh * D);
         __syncthreads();
+        if (k0 > wrow_last) continue;  // the whole tile is above this warp's rows
+        // ---- scores: lane holds keys kA = k0 + lane and kB = k0 + 32 + lane
+        // against every row of the warp (each K read feeds kRowsPerWarp rows).
+        float sA[kRowsPerWarp], sB[kRowsPerWarp];
 #pragma unroll
-        for (int grp = 0; grp < kRowsPerWarp / kRowGroup; ++grp) {
-            const int lr0 = wr0 + grp * kRowGroup;           // local row of the group
-            const uint32_t grow_last = q0 + lr0 + kRowGroup - 1;
-#pragma unroll
-            for (int half = 0; half < kBN / 32; ++half) {
-                const uint32_t key0 = k0 + half * 32;
-                if (key0 > grow_last) continue;              // whole slice above the diagonal
-                const int kl = half * 32 + lane;             // this lane's key (local)
-                const uint32_t key = k0 + kl;
-                float s[kRowGroup];
-#pragma unroll
-                for (int r = 0; r < kRowGroup; ++r) s[r] = 0.f;
-#pragma unroll 8
-                for (int d4 = 0; d4 < D / 4; ++d4) {
-                    const float4 kk = *reinterpret_cast<const float4*>(&sm.k[kl][d4 * 4]);
-#pragma unroll
-                    for (int r = 0; r < kRowGroup; ++r) {
-                        const float4 qq = *reinterpret_cast<const float4*>(&sm.q[lr0 + r][d4 * 4]);
-                        s[r] = fmaf(qq.x, kk.x, s[r]);
-                        s[r] = fmaf(qq.y, kk.y, s[r]);
-                        s[r] = fmaf(qq.z, kk.z, s[r]);
-                        s[r] = fmaf(qq.w, kk.w, s[r]);
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < kRowGroup; ++r) {
-                    const int ri = grp * kRowGroup + r;
-                    const uint32_t row = q0 + lr0 + r;
-                    float sc = (key <= row) ? s[r] * scale_log2 : -CUDART_INF_F;
-                    float mx = sc;
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    const float m_new = fmaxf(mrow[ri], mx);
-                    if (m_new == -CUDART_INF_F) { s[r] = 0.f; continue; }  // nothing attended yet
-                    const float corr = exp2f(mrow[ri] - m_new);
-                    const float p = exp2f(sc - m_new);
-                    float ps = p;
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-                        ps += __shfl_xor_sync(0xffffffffu, ps, off);
-                    lrow[ri] = fmaf(lrow[ri], corr, ps);
-                    mrow[ri] = m_new;
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc[ri][e] *= corr;
-                    s[r] = p;
-                }
-                // PV over the 32 keys of the slice
+        for (int r = 0; r < kRowsPerWarp; ++r) sA[r] = sB[r] = 0.f;
 #pragma unroll 4
-                for (int j = 0; j < 32; ++j) {
-                    const float* vrow = &sm.v[half * 32 + j][lane * VEC];
-                    float vv[VEC];
-                    if constexpr (VEC == 4) {
-                        const float4 t4 = *reinterpret_cast<const float4*>(vrow);
-                        vv[0] = t4.x; vv[1] = t4.y; vv[2] = t4.z; vv[3] = t4.w;
-                    } else if constexpr (VEC == 2) {
-                        const float2 t2 = *reinterpret_cast<const float2*>(vrow);
-                        vv[0] = t2.x; vv[1] = t2.y;
-                    } else {
-                        vv[0] = vrow[0];
-                    }
+        for (int d4 = 0; d4 < D / 4; ++d4) {
+            const float4 ka = *reinterpret_cast<const float4*>(&sm.k[lane][d4 * 4]);
+            const float4 kb = *reinterpret_cast<const float4*>(&sm.k[32 + lane][d4 * 4]);
 #pragma unroll
-                    for (int r = 0; r < kRowGroup; ++r) {
-                        const float pj = __shfl_sync(0xffffffffu, s[r], j);
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                const float4 qq = *reinterpret_cast<const float4*>(&sm.q[wr0 + r][d4 * 4]);
+                sA[r] = fmaf(qq.x, ka.x, sA[r]);
+                sA[r] = fmaf(qq.y, ka.y, sA[r]);
+                sA[r] = fmaf(qq.z, ka.z, sA[r]);
+                sA[r] = fmaf(qq.w, ka.w, sA[r]);
+                sB[r] = fmaf(qq.x, kb.x, sB[r]);
+                sB[r] = fmaf(qq.y, kb.y, sB[r]);
+                sB[r] = fmaf(qq.z, kb.z, sB[r]);
+                sB[r] = fmaf(qq.w, kb.w, sB[r]);
+            }
+        }
+        // ---- online softmax per row over the tile's 64 keys (base 2)
+        const uint32_t keyA = k0 + lane, keyB = k0 + 32 + lane;
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e)
-                            acc[grp * kRowGroup + r][e] = fmaf(pj, vv[e], acc[grp * kRowGroup + r][e]);
-                    }
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const uint32_t row = q0 + wr0 + r;
+            const float a = keyA <= row ? sA[r] * scale_log2 : -CUDART_INF_F;
+            const float b = keyB <= row ? sB[r] * scale_log2 : -CUDART_INF_F;
+            float mx = fmaxf(a, b);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(mrow[r], mx);
+            float pa = 0.f, pb = 0.f, corr = 1.f;
+            if (m_new != -CUDART_INF_F) {  // some key attended so far
+                corr = exp2f(mrow[r] - m_new);
+                pa = exp2f(a - m_new);
+                pb = exp2f(b - m_new);
+            }
+            float ps = pa + pb;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+            lrow[r] = fmaf(lrow[r], corr, ps);
+            mrow[r] = m_new;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[r][e] *= corr;
+            sA[r] = pa;  // the weights, kept for the P.V update
+            sB[r] = pb;
+        }
+        // ---- O += P V, one 32-key half at a time (a half entirely above the
+        // warp's rows is skipped; inside a half the weights of keys past a
+        // row's diagonal are 0)
+#pragma unroll
+        for (int half = 0; half < kBN / 32; ++half) {
+            if (k0 + half * 32 > wrow_last) break;
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) {
+                const float* vrow = &sm.v[half * 32 + j][lane * VEC];
+                float vv[VEC];
+                if constexpr (VEC == 4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(vrow);
+                    vv[0] = t4.x; vv[1] = t4.y; vv[2] = t4.z; vv[3] = t4.w;
+                } else if constexpr (VEC == 2) {
+                    const float2 t2 = *reinterpret_cast<const float2*>(vrow);
+                    vv[0] = t2.x; vv[1] = t2.y;
+                } else {
+                    vv[0] = vrow[0];
+                }
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r) {
+                    const float pj = __shfl_sync(0xffffffffu, half == 0 ? sA[r] : sB[r], j);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[r][e] = fmaf(pj, vv[e], acc[r][e]);
                 }
             }
         }
