@@ -70,6 +70,15 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kWarpsPerSm = ATTN_DECODE_WARPS_PER_SM;     // occupancy the plan aims for
 constexpr int kMinBlocks = kWarpsPerSm / kWarps > 0 ? kWarpsPerSm / kWarps : 1;
 constexpr int kRowsPerStep = 4;  // K/V rows a warp holds per step
+// L2 prefetch lead: a warp asks L2 for the K/V rows this many rows ahead of
+// the step it computes (one bulk prefetch per step, no registers or shared
+// memory).  Measured on long caches: one step ahead streams at the copy
+// rate; leads of 8 rows and more lose 5-40%, and an unbounded prefetch of
+// the whole range (more than L2 holds) evicts rows before they are read.
+#ifndef ATTN_DECODE_PREFETCH_LEAD
+#define ATTN_DECODE_PREFETCH_LEAD 4
+#endif
+constexpr uint32_t kPrefetchLead = ATTN_DECODE_PREFETCH_LEAD;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaskScore = -1.0e4f;  // the page's replaced score
 constexpr uint32_t kNoRow = 0xffffffffu;
@@ -213,7 +222,10 @@ __device__ __forceinline__ float finish(float M, float L, float O, uint32_t wind
     return O / L;
 }
 
-template <int D, int GP>
+// ROLL: keep the L2 prefetch running ahead inside the step loop.  Launched
+// only when a warp walks more than kPrefetchLead rows: the extra code costs
+// the 128-register builds a spill, which a one-step walk should not pay.
+template <int D, int GP, bool ROLL>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const DecodeArgs a) {
     constexpr int V = D / 32;    // elements of a row per lane
     constexpr int U = kRowsPerStep;
@@ -244,12 +256,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
 
     // The launch is a programmatic dependent of the previous kernel on the
     // stream, so this CTA may start while that kernel drains.  Until the
-    // grid dependency resolves it only warms L2 with its K/V rows (a bulk
+    // grid dependency resolves it only warms L2 with its first K/V rows (a bulk
     // prefetch reads memory without using it, and L2 is coherent, so a row
     // written by the previous kernel is still read fresh below); every read
     // of data and every write waits for the previous kernel's completion.
-    if (lane == 0 && r1 > r0) {
-        const uint32_t bytes = (r1 - r0) * (uint32_t)D * 4u;
+    if (lane == 0 && r1 > r0 && kPrefetchLead > 0) {
+        const uint32_t bytes = min(r1 - r0, kPrefetchLead) * (uint32_t)D * 4u;
         bulk_prefetch_l2(a.k_cache + kv_base + (size_t)r0 * D, bytes);
         bulk_prefetch_l2(a.v_cache + kv_base + (size_t)r0 * D, bytes);
     }
@@ -318,6 +330,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) decode_kernel(const Deco
         for (int e = 0; e < V; ++e) o[g][e] = 0.f;
 
     for (uint32_t base = r0; base < r1; base += U) {
+        // Keep the L2 prefetch kPrefetchLead rows ahead of this step.
+        if (ROLL && base + kPrefetchLead < r1) {
+            if (lane == 0) {
+                const uint32_t pf = base + kPrefetchLead;
+                const uint32_t bytes = min(r1 - pf, (uint32_t)U) * (uint32_t)D * 4u;
+                bulk_prefetch_l2(a.k_cache + kv_base + (size_t)pf * D, bytes);
+                bulk_prefetch_l2(a.v_cache + kv_base + (size_t)pf * D, bytes);
+            }
+            __syncwarp();
+        }
         if (own_new) {
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -586,7 +608,9 @@ cudaError_t launch_gp(const DecodeArgs& a, const DecodePlan& plan, uint32_t kv_h
     dcfg.stream = stream;
     dcfg.attrs = attr;
     dcfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&dcfg, decode_kernel<D, GP>, a);
+    const bool roll = kPrefetchLead > 0 && plan.rows_per_warp > kPrefetchLead;
+    cudaError_t e = cudaLaunchKernelEx(&dcfg, roll ? decode_kernel<D, GP, true>
+                                                   : decode_kernel<D, GP, false>, a);
     if (e != cudaSuccess || plan.n_splits == 1) return e;
     CombineArgs c{};
     c.part_o = a.part_o;

@@ -403,8 +403,8 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
 # ---------------------------------------------------------------- companion workloads
 
 def bench_decode_companion(attn, shape, device, stream, steps, peaks, peak_src):
-    """The windowed decode after an append (32 query heads over 8 KV heads,
-    a 32768-row cache, window 4096): one step = attn_decode_append at
+    """A decode after an append (32 query heads over 8 KV heads, a
+    32768-row cache, window 4096 or none): one step = attn_decode_append at
     total_seq-1.  L2-cold through cache replicas sized by the live bytes."""
     db = DecodeBench(attn, shape, device)
     err = db.check()
@@ -615,6 +615,15 @@ def our_arm(args):
         if rank == 0:
             print(json.dumps({"only": args.only, "prefill": [res]}), flush=True)
         return 0
+    if args.only in ("decode_32k_window", "decode_32k_stream"):
+        # Profiling aid: one 32768-row decode workload alone (no headline line).
+        cs = (workloads.DECODE_32K_WINDOW if args.only == "decode_32k_window"
+              else workloads.DECODE_32K_STREAM)
+        res = bench_decode_companion(attn, cs, device, stream,
+                                     2000 if cs.window else 200, peaks, peak_src)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "other_workloads": [res]}), flush=True)
+        return 0
     shape = workloads.DECODE_4K
     db = DecodeBench(attn, shape, device)
     err = db.check()
@@ -715,6 +724,8 @@ def our_arm(args):
         layer_stack = bench_layer_stack(attn, workloads.PREFILL_2K, device, stream)
         companions.append(bench_decode_companion(attn, workloads.DECODE_32K_WINDOW, device,
                                                  stream, 2000, peaks, peak_src))
+        companions.append(bench_decode_companion(attn, workloads.DECODE_32K_STREAM, device,
+                                                 stream, 200, peaks, peak_src))
         companions.append(bench_prefill_fp32_small(attn, workloads.PREFILL_SMALL, device,
                                                    stream, 3200, peaks))
 
@@ -780,7 +791,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "prefill_2k", "prefill_16k"],
+    ap.add_argument("--only", choices=["all", "decode", "prefill_2k", "prefill_16k",
+                                       "decode_32k_window", "decode_32k_stream"],
                     default="all", help="profiling aid: run one workload only")
     args = ap.parse_args(argv)
     if args.warmup < 3:

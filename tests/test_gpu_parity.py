@@ -453,6 +453,31 @@ def test_decode_append_position_inside_the_cache(attn):
     assert amax <= FP32_ABS and rel <= FP32_REL
 
 
+def test_workload_append_then_streaming_decode_32k(attn):
+    """The fused append + decode over a full 32768-row cache (no window),
+    268 MB of K/V, as the bench times it: every warp runs many steps with
+    the L2 prefetch running ahead of its loads."""
+    c = workloads.DECODE_32K_STREAM
+    q, kc, vc, kn, vn = workloads.shape_inputs(c)
+    dk, dv = kc.cuda(), vc.cuda()
+    pos = c.total_seq - 1
+    buf, out = guarded_empty(c.num_heads * c.head_dim)
+    attn.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), dk, dv, out, c.num_heads,
+                            c.kv_heads, c.head_dim, c.max_seq, c.total_seq, pos,
+                            window=c.window)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    assert guards_intact(buf)
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    ref = oracle.decode_append(q.numpy(), kn.numpy(), vn.numpy(), kh, vh, c.num_heads,
+                               c.kv_heads, c.head_dim, c.max_seq, c.total_seq, pos)
+    np.testing.assert_array_equal(dk[:, pos].cpu().numpy(), kh[:, pos])
+    np.testing.assert_array_equal(dv[:, pos].cpu().numpy(), vh[:, pos])
+    amax, rel = compare(out.view(c.num_heads, c.head_dim).cpu().numpy(), ref)
+    print(f"{c.name}: max abs {amax:.3e} rel {rel:.3e}")
+    assert amax <= FP32_ABS and rel <= FP32_REL
+
+
 def test_decode_append_equals_unfused_append_then_decode(attn):
     """The fused entry point and kv_append + attn_decode agree to fp32 rounding."""
     c = workloads.DECODE_32K_WINDOW

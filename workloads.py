@@ -82,6 +82,10 @@ DECODE_32K_WINDOW = DecodeShape("append_decode_h32x8_d128_t32768_w4096", 32, 8, 
                                 32768, 4096, seed=3, append=True)
 PREFILL_16K = PrefillShape("prefill_m16384_h28x4_d128", 16384, 28, 4, 128, 3584, 512, seed=4,
                            mul=0.5, tensor_core=True)
+# Decode over a full 32768-row cache with no window: 268 MB of K/V per step,
+# more than L2 holds, so every step streams from HBM.
+DECODE_32K_STREAM = DecodeShape("append_decode_h32x8_d128_t32768", 32, 8, 128, 32768, 32768, 0,
+                                seed=5, append=True)
 
 ALL = [PREFILL_SMALL, DECODE_4K, PREFILL_2K, DECODE_32K_WINDOW, PREFILL_16K]
 BY_NAME = {c.name: c for c in ALL}
