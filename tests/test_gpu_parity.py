@@ -216,6 +216,27 @@ def test_prefill_padded_strides(attn, prec):
 
 
 @pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_stride_padding_is_never_read(attn, prec, d):
+    """NaN in the padding columns between rows (past Hq*D in Q, past Hkv*D in
+    K and V) must not reach the output: only the heads' columns are read."""
+    m, hq, hkv = 333, 6, 2
+    qs, kvs = hq * d + 64, hkv * d + 128
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, 71)
+    q[:, hq * d:] = float("nan")
+    k[:, hkv * d:] = float("nan")
+    v[:, hkv * d:] = float("nan")
+    got = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, prec)
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs)
+    assert np.isfinite(ref).all() and np.isfinite(got).all()
+    amax, rel = compare(got, ref)
+    if prec == FP32:
+        assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
+    else:
+        assert amax <= TC_ABS, amax
+
+
+@pytest.mark.parametrize("prec", [FP16, FP32])
 def test_prefill_single_packed_buffer(attn, prec):
     """Q, K, V as column slices of one [M, (Hq+2Hkv)D] projection output with
     equal strides (the page's zero-copy packed layout)."""
@@ -476,6 +497,43 @@ def test_workload_append_then_streaming_decode_32k(attn):
     amax, rel = compare(out.view(c.num_heads, c.head_dim).cpu().numpy(), ref)
     print(f"{c.name}: max abs {amax:.3e} rel {rel:.3e}")
     assert amax <= FP32_ABS and rel <= FP32_REL
+
+
+@pytest.mark.parametrize("hq,hkv,d,S,T,W", [
+    (12, 2, 128, 4200, 4097, 0),     # one step per warp, ragged tail
+    (12, 2, 128, 40000, 33333, 0),   # many steps per warp (L2 prefetch ahead)
+    (32, 8, 64, 9000, 8191, 1000),   # window: K rows below its start poisoned too
+    (6, 1, 32, 64, 5, 0),
+    (8, 8, 128, 300, 1, 0),
+])
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_rows_outside_the_live_range_are_never_read(attn, hq, hkv, d, S, T, W, fused):
+    """Cache rows at or past total_seq are not part of the attention, and the
+    keys of rows below the window start are replaced by the -1e4 score: NaN in
+    either must not reach the output."""
+    q, kc, vc, kn, vn = workloads.decode_inputs(hq, hkv, d, S, seed=T + W, append=True)
+    kc[:, T:] = float("nan")
+    vc[:, T:] = float("nan")
+    ws = T - W if (W > 0 and T > W) else 0
+    kc[:, :ws] = float("nan")
+    dk, dv = kc.cuda(), vc.cuda()
+    buf, out = guarded_empty(hq * d)
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    if fused:
+        attn.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), dk, dv, out, hq, hkv, d, S, T,
+                                T - 1, window=W)
+        ref = oracle.decode_append(q.numpy(), kn.numpy(), vn.numpy(), kh, vh, hq, hkv, d, S, T,
+                                   T - 1, window=W)
+    else:
+        attn.attn_decode(q.cuda(), dk, dv, out, hq, hkv, d, S, T, window=W)
+        ref = oracle.decode(q.numpy(), kh, vh, hq, hkv, d, S, T, W)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    assert guards_intact(buf)
+    got = out.view(hq, d).cpu().numpy()
+    assert np.isfinite(ref).all() and np.isfinite(got).all()
+    amax, rel = compare(got, ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
 
 
 def test_decode_append_equals_unfused_append_then_decode(attn):
