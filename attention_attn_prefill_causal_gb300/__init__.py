@@ -107,8 +107,23 @@ def _workspace(nbytes: int, like, workspace):
     if workspace is not None or nbytes == 0:
         return workspace
     import torch
-    dev = like.device if hasattr(like, "device") else torch.device("cuda", torch.cuda.current_device())
+    dev = like.device if getattr(like, "is_cuda", False) else torch.device(
+        "cuda", torch.cuda.current_device())
     return torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+
+def _workspace_args(workspace, workspace_bytes, size_fn, like):
+    """(workspace, bytes) for a call: the caller's buffer and its size (the
+    size query runs only when the library must allocate or the size is not
+    known), or a new device buffer of the size the call needs."""
+    if workspace is None:
+        need = size_fn()
+        workspace = _workspace(need, like, None)
+        return workspace, need
+    if workspace_bytes is None:
+        workspace_bytes = (workspace.numel() * workspace.element_size()
+                           if hasattr(workspace, "numel") else size_fn())
+    return workspace, workspace_bytes
 
 
 def attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim, precision=ATTN_PREC_FP16):
@@ -124,11 +139,9 @@ def attn_prefill_causal(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_st
                         stream=None, check=True):
     """Causal GQA prefill (C: attn_prefill_causal).  q/o: [m, q_stride] fp32,
     k/v: [m, kv_stride] fp32.  Returns the status (raises when ``check``)."""
-    need = attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim, precision)
-    workspace = _workspace(need, q, workspace)
-    if workspace_bytes is None:
-        workspace_bytes = (workspace.numel() * workspace.element_size()
-                           if hasattr(workspace, "numel") else need)
+    workspace, workspace_bytes = _workspace_args(
+        workspace, workspace_bytes,
+        lambda: attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim, precision), q)
     st = lib.attn_prefill_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(o), m, num_q_heads, num_kv_heads,
                                  head_dim, q_stride, kv_stride, float(scale), int(precision),
                                  _ptr(workspace), workspace_bytes, _stream(stream))
@@ -139,11 +152,10 @@ def attn_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq
                 window=0, scale=0.0, workspace=None, workspace_bytes=None, stream=None, check=True):
     """Single-query GQA decode (C: attn_decode).  q/out: [num_heads, head_dim];
     caches: [kv_heads, max_seq, head_dim].  Returns the status."""
-    need = attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window)
-    workspace = _workspace(need, q, workspace)
-    if workspace_bytes is None:
-        workspace_bytes = (workspace.numel() * workspace.element_size()
-                           if hasattr(workspace, "numel") else need)
+    workspace, workspace_bytes = _workspace_args(
+        workspace, workspace_bytes,
+        lambda: attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window),
+        k_cache)
     st = lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, kv_heads,
                          head_dim, max_seq, total_seq, window, float(scale), _ptr(workspace),
                          workspace_bytes, _stream(stream))
@@ -155,11 +167,10 @@ def attn_decode_append(q, k_new, v_new, k_cache, v_cache, out, num_heads, kv_hea
                        rope_sin=None, workspace=None, workspace_bytes=None, stream=None,
                        check=True):
     """Fused (RoPE +) append + decode (C: attn_decode_append)."""
-    need = attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window)
-    workspace = _workspace(need, q, workspace)
-    if workspace_bytes is None:
-        workspace_bytes = (workspace.numel() * workspace.element_size()
-                           if hasattr(workspace, "numel") else need)
+    workspace, workspace_bytes = _workspace_args(
+        workspace, workspace_bytes,
+        lambda: attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window),
+        k_cache)
     st = lib.attn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin),
                                 _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, kv_heads,
                                 head_dim, max_seq, total_seq, position, window, float(scale),

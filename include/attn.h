@@ -7,6 +7,15 @@
  *  - All tensor pointers are DEVICE pointers to fp32 data unless stated.  The
  *    caller owns every buffer (inputs, outputs, caches, workspaces); the
  *    library never allocates, frees or retains caller memory.
+ *  - Host-resident step buffers.  The decode entry points and kv_append also
+ *    accept their small per-step buffers -- q, out, k_new, v_new, rope_cos,
+ *    rope_sin, k_src, v_src -- in page-locked host memory that the device
+ *    addresses directly (cudaHostAlloc / cudaMallocHost under unified
+ *    addressing, or cudaHostRegister with cudaHostRegisterMapped).  The
+ *    kernels then read and write those bytes over the CPU-GPU link in the
+ *    call itself, with no separate copy.  Caches, workspaces and every
+ *    prefill buffer must be device memory (they are moved with TMA and bulk
+ *    copies).  Pageable host memory is not supported anywhere.
  *  - Every compute call is asynchronous on `stream` (a cudaStream_t passed as
  *    void*; NULL = the legacy default stream).  Results are ready when the
  *    stream reaches the call.  No call synchronises the host except

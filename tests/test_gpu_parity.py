@@ -460,6 +460,49 @@ def test_decode_append_matches_oracle(attn, rope, hq, hkv, d, S, T, W):
     assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
 
 
+@pytest.mark.parametrize("rope", [False, True])
+@pytest.mark.parametrize("hq,hkv,d,S,T,W", [(12, 2, 128, 4096, 4096, 0),
+                                            (32, 8, 64, 9000, 8191, 1000)])
+def test_decode_with_host_resident_step_buffers(attn, rope, hq, hkv, d, S, T, W):
+    """q, k_new, v_new, the RoPE tables and out in page-locked host memory:
+    the kernels read and write them directly.  The result equals the call on
+    device copies of the same buffers bit for bit, and the oracle."""
+    q, kc, vc, kn, vn = workloads.decode_inputs(hq, hkv, d, S, seed=hq + T, append=True)
+    cos = sin = None
+    if rope:
+        cos, sin = _rope_tables(d, T)
+    pos = T - 1
+    hq_, hkn, hvn = q.pin_memory(), kn.pin_memory(), vn.pin_memory()
+    hcos = torch.from_numpy(cos).pin_memory() if rope else None
+    hsin = torch.from_numpy(sin).pin_memory() if rope else None
+    hout = torch.full((hq, d), float("nan")).pin_memory()
+    dk1, dv1, dk2, dv2 = kc.cuda(), vc.cuda(), kc.cuda(), vc.cuda()
+    dout = torch.empty(hq, d, device="cuda")
+    attn.attn_decode_append(hq_, hkn, hvn, dk1, dv1, hout, hq, hkv, d, S, T, pos, window=W,
+                            rope_cos=hcos, rope_sin=hsin)
+    attn.attn_decode_append(q.cuda(), kn.cuda(), vn.cuda(), dk2, dv2, dout, hq, hkv, d, S, T,
+                            pos, window=W,
+                            rope_cos=hcos.cuda() if rope else None,
+                            rope_sin=hsin.cuda() if rope else None)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    assert torch.equal(hout, dout.cpu())
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    kh, vh = kc.numpy().copy(), vc.numpy().copy()
+    ref = oracle.decode_append(q.numpy(), kn.numpy(), vn.numpy(), kh, vh, hq, hkv, d, S, T, pos,
+                               window=W, rope_cos=cos, rope_sin=sin)
+    amax, rel = compare(hout.numpy(), ref)
+    assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
+    # the plain decode and the separate append take host buffers the same way
+    hout2 = torch.full((hq, d), float("nan")).pin_memory()
+    attn.kv_append(hkn, hvn, dk2, dv2, hkv, d, S, pos)
+    attn.attn_decode(hq_, dk2, dv2, hout2, hq, hkv, d, S, T, window=W)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    if not rope:
+        assert (hout2 - hout).abs().max().item() <= 1e-6
+
+
 def test_decode_append_position_inside_the_cache(attn):
     """An append in the middle of the attended range replaces that row."""
     hq, hkv, d, S, T = 8, 2, 128, 512, 500
