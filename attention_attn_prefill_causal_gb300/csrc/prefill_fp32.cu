@@ -95,6 +95,11 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     const uint32_t kvh = h / heads_per_kv;
     const uint32_t q0 = qb * kBM;
 
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream: the CTA may be resident before that kernel finishes, so every
+    // global read and write comes after the grid dependency resolves.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     load_tile<D>(sm.q, q, q0, m, q_stride, h * D, kBM);
 
     float mrow[kRowsPerWarp], lrow[kRowsPerWarp], acc[kRowsPerWarp][VEC];
@@ -220,10 +225,18 @@ cudaError_t launch_bm(const float* q, const float* k, const float* v, float* o, 
     const int smem = (int)sizeof(Smem<D, BM>);
     const cudaError_t e = ensure_dynamic_smem<prefill_fp32_kernel<D, BM>>(smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((m + BM - 1) / BM, num_q_heads);
-    prefill_fp32_kernel<D, BM><<<grid, kThreads, smem, stream>>>(
-        q, k, v, o, m, num_q_heads / num_kv_heads, q_stride, kv_stride, scale * kLog2e);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((m + BM - 1) / BM, num_q_heads, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_fp32_kernel<D, BM>, q, k, v, o, m,
+                              num_q_heads / num_kv_heads, q_stride, kv_stride, scale * kLog2e);
 }
 
 template <int D>

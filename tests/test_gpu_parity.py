@@ -626,6 +626,38 @@ def test_decode_waits_for_the_kernel_before_it(attn):
         assert amax <= FP32_ABS and rel <= FP32_REL
 
 
+def test_prefill_fp32_waits_for_the_kernel_before_it(attn):
+    """The exact-mode prefill launches as a programmatic dependent of the
+    previous kernel on the stream.  Here the kernels right before the second
+    call rewrite Q, K and V, and the call right after reads the first call's
+    output as its Q: every call must see the values of the kernel before it."""
+    m, hq, hkv, d = 64, 4, 2, 32
+    qs, kvs = 128, 64
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, 0)
+    q2, k2, v2 = workloads.prefill_inputs(m, qs, kvs, 1)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    outs = [torch.full((m, qs), float("nan"), device="cuda") for _ in range(3)]
+    torch.cuda.synchronize()
+    attn.attn_prefill_causal(dq, dk, dv, outs[0], m, hq, hkv, d, qs, kvs,
+                             precision=attn.ATTN_PREC_FP32)
+    dq.copy_(q2.cuda())                # predecessor kernels of the next call
+    dk.copy_(k2.cuda())
+    dv.copy_(v2.cuda())
+    attn.attn_prefill_causal(dq, dk, dv, outs[1], m, hq, hkv, d, qs, kvs,
+                             precision=attn.ATTN_PREC_FP32)
+    attn.attn_prefill_causal(outs[1], dk, dv, outs[2], m, hq, hkv, d, qs, kvs,
+                             precision=attn.ATTN_PREC_FP32)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    ref0 = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs)
+    ref1 = oracle.prefill_causal(q2.numpy(), k2.numpy(), v2.numpy(), m, hq, hkv, d, qs, kvs)
+    o1 = outs[1].cpu().numpy()
+    ref2 = oracle.prefill_causal(o1, k2.numpy(), v2.numpy(), m, hq, hkv, d, qs, kvs)
+    for got, ref in ((outs[0], ref0), (outs[1], ref1), (outs[2], ref2)):
+        amax, rel = compare(heads_view(got.reshape(-1), m, qs, hq, d), ref)
+        assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
+
+
 def test_decode_workspace_reuse(attn):
     """One workspace, never cleared, serves many calls of different shapes."""
     ws = torch.full((8 << 20,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN garbage
