@@ -273,6 +273,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             load_q32(0);
             load_q32(1);
             q_issued = 2;
+            // The kernel is a programmatic dependent of the rounding pre-pass.
+            // Q is the caller's (its writer finished before the pre-pass
+            // began), so it is staged at once; the fp16 K and V the pre-pass
+            // writes are read only once that grid has completed.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             bool ok = mbar_wait(smem_u32(&bars.q_ready[0]), 0, wait_ns, status, kStatusTimeout);
             if (ok && n_kv_all > 0) {
                 load_k(0);
@@ -587,6 +592,7 @@ __global__ void __launch_bounds__(256)
 prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
                        uint32_t num_q_heads, uint32_t q_stride) {
     constexpr uint32_t kPerRow = D / 8;  // threads per (row, head)
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
     const uint32_t item = tid / kPerRow, e0 = (tid % kPerRow) * 8;
@@ -656,6 +662,13 @@ __global__ void round_operands_kernel(const float* __restrict__ k, const float* 
                                       uint16_t* __restrict__ kh, uint16_t* __restrict__ vh,
                                       uint32_t m, uint32_t kv_cols, uint32_t kv_stride,
                                       unsigned int* status) {
+    // Launched as a programmatic dependent of the kernel before it: wait for
+    // that grid before any global access.  Only then may the prefill kernel
+    // launch (it stages the caller's Q before its own wait, so every kernel
+    // before this one must have completed); it reads the rounded K and V
+    // only after this grid has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const float* src = blockIdx.y == 0 ? k : v;
     uint16_t* dst = blockIdx.y == 0 ? kh : vh;
     const uint32_t cols = kv_cols;
@@ -811,9 +824,17 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
         const size_t work = (size_t)m * kv_cols / 8;
         const uint32_t threads = 256;
         uint32_t blocks = (uint32_t)std::min<size_t>((work + threads - 1) / threads, 4096);
-        round_operands_kernel<BF16><<<dim3(blocks, 2), threads, 0, stream>>>(
-            k, v, kh, vh, m, kv_cols, kv_stride, status);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchAttribute pattr[1];
+        pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pattr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3(blocks, 2, 1);
+        pcfg.blockDim = dim3(threads, 1, 1);
+        pcfg.stream = stream;
+        pcfg.attrs = pattr;
+        pcfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&pcfg, round_operands_kernel<BF16>, k, v, kh, vh, m,
+                                           kv_cols, kv_stride, status);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tq, tk, tv, to, tpo;
@@ -834,23 +855,29 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
         const cudaError_t e = ensure_dynamic_smem<prefill_tc_kernel<D, BF16>>((int)L::kSmemAlloc);
         if (e != cudaSuccess) return e;
     }
-    prefill_tc_kernel<D, BF16><<<plan.n_items * num_q_heads, kThreads, L::kSmemAlloc, stream>>>(
-        tq, tk, tv, to, tpo, m, num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e, status,
-        wait_ns, split);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;
-    const uint32_t rows = m - split.first_split_row;
-    const uint64_t threads = (uint64_t)rows * num_q_heads * (D / 8);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((uint32_t)((threads + 255) / 256), 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.n_items * num_q_heads, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kSmemAlloc;
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_combine_kernel<D>, split, o, m, num_q_heads, q_stride);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, BF16>, tq, tk, tv, to, tpo, m,
+                                       num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e,
+                                       status, wait_ns, split);
+    if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;
+    const uint32_t rows = m - split.first_split_row;
+    const uint64_t threads = (uint64_t)rows * num_q_heads * (D / 8);
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3((uint32_t)((threads + 255) / 256), 1, 1);
+    ccfg.blockDim = dim3(256, 1, 1);
+    ccfg.stream = stream;
+    ccfg.attrs = attr;
+    ccfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&ccfg, prefill_combine_kernel<D>, split, o, m, num_q_heads, q_stride);
 }
 
 }  // namespace

@@ -658,6 +658,38 @@ def test_prefill_fp32_waits_for_the_kernel_before_it(attn):
         assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
 
 
+def test_prefill_tc_waits_for_the_kernels_before_it(attn):
+    """The tensor-core prefill chains its kernels as programmatic dependents
+    (rounding pre-pass, main kernel staging the caller's Q before it waits
+    for the pre-pass, combine), and its pre-pass depends the same way on the
+    kernel before the call.  Back-to-back calls where the kernels right
+    before a call rewrite K and V, and where a call's Q is the previous
+    call's output (written by that call's combine kernel), must see the new
+    values."""
+    m, hq, hkv, d = 2048, 12, 2, 128    # splits its key walk: the combine runs last
+    qs, kvs = hq * d, hkv * d
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, 2)
+    q2, k2, v2 = workloads.prefill_inputs(m, qs, kvs, 3)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    outs = [torch.full((m, qs), float("nan"), device="cuda") for _ in range(3)]
+    torch.cuda.synchronize()
+    attn.attn_prefill_causal(dq, dk, dv, outs[0], m, hq, hkv, d, qs, kvs)
+    dk.copy_(k2.cuda())                # predecessor kernels of the next call
+    dv.copy_(v2.cuda())
+    attn.attn_prefill_causal(dq, dk, dv, outs[1], m, hq, hkv, d, qs, kvs)
+    attn.attn_prefill_causal(outs[1], dk, dv, outs[2], m, hq, hkv, d, qs, kvs)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == attn.ATTN_OK
+    rows = workloads.sample_rows(m, 5, 16, 16, 48)
+    o1 = outs[1].cpu().numpy()
+    refs = (oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs, rows=rows),
+            oracle.prefill_causal(q.numpy(), k2.numpy(), v2.numpy(), m, hq, hkv, d, qs, kvs, rows=rows),
+            oracle.prefill_causal(o1, k2.numpy(), v2.numpy(), m, hq, hkv, d, qs, kvs, rows=rows))
+    for got, ref in zip(outs, refs):
+        amax, _ = compare(heads_view(got.reshape(-1), m, qs, hq, d)[rows], ref)
+        assert amax <= TC_ABS, amax
+
+
 def test_decode_workspace_reuse(attn):
     """One workspace, never cleared, serves many calls of different shapes."""
     ws = torch.full((8 << 20,), 0xFF, dtype=torch.uint8, device="cuda")  # NaN garbage
