@@ -38,8 +38,13 @@
 //    log-sum-exp and normalises.
 //  * Consecutive calls overlap: each decode launch is a programmatic
 //    dependent of the kernel before it on the stream, and its CTAs prefetch
-//    their K/V rows into L2 while that kernel drains, then wait for it
-//    before reading anything.
+//    their first step's K/V rows into L2 while that kernel drains, then wait
+//    for it before reading anything.  A warp that walks more than one step
+//    keeps a bulk L2 prefetch one step ahead of its register loads (the ROLL
+//    build); prefetching a whole long range at once would overfill L2.
+//  * q, k_new, v_new, the RoPE tables and out are read and written with
+//    plain loads and stores, so they may also sit in page-locked host memory
+//    (read over the CPU-GPU link inside the call).
 //  * Positions below window_start are never read; their score is -1e4
 //    exactly as on the page, and the final merge adds their weight
 //    exp(-1e4 - max) back.  That weight is zero in fp32 unless every live
