@@ -20,9 +20,10 @@
 //  * per row, the tile's max and sum come from warp shuffles; the online
 //    softmax runs in base 2 (scores pre-multiplied by log2 e, as the page
 //    does before ex2);
-//  * for PV each lane owns head_dim/32 output elements and takes the
-//    weights by shuffle, one 32-key half at a time (a half entirely above
-//    the warp's rows is skipped).
+//  * for PV each warp writes its weights to shared memory over the K tile
+//    (free once every warp's dot products are done); each lane owns
+//    head_dim/32 output elements and reads four keys' weights of a row with
+//    one broadcast 128-bit load, stopping at the warp's last attended key.
 // Causal masking is the loop bound plus a per-key test on the diagonal tile.
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -115,87 +116,108 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     const uint32_t last_row = min(q0 + kBM, m) - 1;
     const uint32_t n_tiles = last_row / kBN + 1;
 
+    // This warp's weights for the current tile, [kRowsPerWarp][kBN], staged
+    // over the K tile once every warp has finished its dot products.
+    float* const sp = &sm.k[0][0] + wr0 * kBN;
     for (uint32_t t = 0; t < n_tiles; ++t) {
         const uint32_t k0 = t * kBN;
-        __syncthreads();
+        __syncthreads();  // the previous tile's P.V no longer reads K (P) or V
         load_tile<D>(sm.k, k, k0, m, kv_stride, kvh * D, kBN);
         load_v_tile<D>(sm.v, v, k0, m, kv_stride, kvh * D);
         __syncthreads();
-        if (k0 > wrow_last) continue;  // the whole tile is above this warp's rows
+        const bool active = k0 <= wrow_last;  // some key of the tile is attended by the warp
         // ---- scores: lane holds keys kA = k0 + lane and kB = k0 + 32 + lane
         // against every row of the warp (each K read feeds kRowsPerWarp rows).
         float sA[kRowsPerWarp], sB[kRowsPerWarp];
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) sA[r] = sB[r] = 0.f;
+        if (active) {
 #pragma unroll 4
-        for (int d4 = 0; d4 < D / 4; ++d4) {
-            const float4 ka = *reinterpret_cast<const float4*>(&sm.k[lane][d4 * 4]);
-            const float4 kb = *reinterpret_cast<const float4*>(&sm.k[32 + lane][d4 * 4]);
-#pragma unroll
-            for (int r = 0; r < kRowsPerWarp; ++r) {
-                const float4 qq = *reinterpret_cast<const float4*>(&sm.q[wr0 + r][d4 * 4]);
-                sA[r] = fmaf(qq.x, ka.x, sA[r]);
-                sA[r] = fmaf(qq.y, ka.y, sA[r]);
-                sA[r] = fmaf(qq.z, ka.z, sA[r]);
-                sA[r] = fmaf(qq.w, ka.w, sA[r]);
-                sB[r] = fmaf(qq.x, kb.x, sB[r]);
-                sB[r] = fmaf(qq.y, kb.y, sB[r]);
-                sB[r] = fmaf(qq.z, kb.z, sB[r]);
-                sB[r] = fmaf(qq.w, kb.w, sB[r]);
-            }
-        }
-        // ---- online softmax per row over the tile's 64 keys (base 2)
-        const uint32_t keyA = k0 + lane, keyB = k0 + 32 + lane;
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) {
-            const uint32_t row = q0 + wr0 + r;
-            const float a = keyA <= row ? sA[r] * scale_log2 : -CUDART_INF_F;
-            const float b = keyB <= row ? sB[r] * scale_log2 : -CUDART_INF_F;
-            float mx = fmaxf(a, b);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(mrow[r], mx);
-            float pa = 0.f, pb = 0.f, corr = 1.f;
-            if (m_new != -CUDART_INF_F) {  // some key attended so far
-                corr = exp2f(mrow[r] - m_new);
-                pa = exp2f(a - m_new);
-                pb = exp2f(b - m_new);
-            }
-            float ps = pa + pb;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-            lrow[r] = fmaf(lrow[r], corr, ps);
-            mrow[r] = m_new;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[r][e] *= corr;
-            sA[r] = pa;  // the weights, kept for the P.V update
-            sB[r] = pb;
-        }
-        // ---- O += P V, one 32-key half at a time (a half entirely above the
-        // warp's rows is skipped; inside a half the weights of keys past a
-        // row's diagonal are 0)
-#pragma unroll
-        for (int half = 0; half < kBN / 32; ++half) {
-            if (k0 + half * 32 > wrow_last) break;
-#pragma unroll 8
-            for (int j = 0; j < 32; ++j) {
-                const float* vrow = &sm.v[half * 32 + j][lane * VEC];
-                float vv[VEC];
-                if constexpr (VEC == 4) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(vrow);
-                    vv[0] = t4.x; vv[1] = t4.y; vv[2] = t4.z; vv[3] = t4.w;
-                } else if constexpr (VEC == 2) {
-                    const float2 t2 = *reinterpret_cast<const float2*>(vrow);
-                    vv[0] = t2.x; vv[1] = t2.y;
-                } else {
-                    vv[0] = vrow[0];
-                }
+            for (int d4 = 0; d4 < D / 4; ++d4) {
+                const float4 ka = *reinterpret_cast<const float4*>(&sm.k[lane][d4 * 4]);
+                const float4 kb = *reinterpret_cast<const float4*>(&sm.k[32 + lane][d4 * 4]);
 #pragma unroll
                 for (int r = 0; r < kRowsPerWarp; ++r) {
-                    const float pj = __shfl_sync(0xffffffffu, half == 0 ? sA[r] : sB[r], j);
+                    const float4 qq = *reinterpret_cast<const float4*>(&sm.q[wr0 + r][d4 * 4]);
+                    sA[r] = fmaf(qq.x, ka.x, sA[r]);
+                    sA[r] = fmaf(qq.y, ka.y, sA[r]);
+                    sA[r] = fmaf(qq.z, ka.z, sA[r]);
+                    sA[r] = fmaf(qq.w, ka.w, sA[r]);
+                    sB[r] = fmaf(qq.x, kb.x, sB[r]);
+                    sB[r] = fmaf(qq.y, kb.y, sB[r]);
+                    sB[r] = fmaf(qq.z, kb.z, sB[r]);
+                    sB[r] = fmaf(qq.w, kb.w, sB[r]);
+                }
+            }
+            // ---- online softmax per row over the tile's 64 keys (base 2)
+            const uint32_t keyA = k0 + lane, keyB = k0 + 32 + lane;
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc[r][e] = fmaf(pj, vv[e], acc[r][e]);
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                const uint32_t row = q0 + wr0 + r;
+                const float a = keyA <= row ? sA[r] * scale_log2 : -CUDART_INF_F;
+                const float b = keyB <= row ? sB[r] * scale_log2 : -CUDART_INF_F;
+                float mx = fmaxf(a, b);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float m_new = fmaxf(mrow[r], mx);
+                float pa = 0.f, pb = 0.f, corr = 1.f;
+                if (m_new != -CUDART_INF_F) {  // some key attended so far
+                    corr = exp2f(mrow[r] - m_new);
+                    pa = exp2f(a - m_new);
+                    pb = exp2f(b - m_new);
+                }
+                float ps = pa + pb;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+                lrow[r] = fmaf(lrow[r], corr, ps);
+                mrow[r] = m_new;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) acc[r][e] *= corr;
+                sA[r] = pa;  // the weights, kept for the P.V update
+                sB[r] = pb;
+            }
+        }
+        __syncthreads();  // every warp's dot products are done: the K tile is free
+        if (!active) continue;
+        // ---- O += P V.  The weights go to shared memory (row r, key j at
+        // sp[r * kBN + j]); each lane then reads four keys' weights of a row
+        // with one broadcast load and its VEC elements of the four V rows.
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            sp[r * kBN + lane] = sA[r];
+            sp[r * kBN + 32 + lane] = sB[r];
+        }
+        __syncwarp();
+        // keys past the warp's last row have weight 0: stop at the last attended one
+        const int jn = (int)min((uint32_t)kBN, wrow_last - k0 + 1);
+#pragma unroll 2
+        for (int j = 0; j < jn; j += 4) {
+            float vv[4][VEC];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float* vrow = &sm.v[j + u][lane * VEC];
+                if constexpr (VEC == 4) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(vrow);
+                    vv[u][0] = t4.x; vv[u][1] = t4.y; vv[u][2] = t4.z; vv[u][3] = t4.w;
+                } else if constexpr (VEC == 2) {
+                    const float2 t2 = *reinterpret_cast<const float2*>(vrow);
+                    vv[u][0] = t2.x; vv[u][1] = t2.y;
+                } else {
+                    vv[u][0] = vrow[0];
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                const float4 p4 = *reinterpret_cast<const float4*>(&sp[r * kBN + j]);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    float a = acc[r][e];
+                    a = fmaf(p4.x, vv[0][e], a);
+                    a = fmaf(p4.y, vv[1][e], a);
+                    a = fmaf(p4.z, vv[2][e], a);
+                    a = fmaf(p4.w, vv[3][e], a);
+                    acc[r][e] = a;
                 }
             }
         }
