@@ -21,11 +21,11 @@
  *    stream reaches the call.  No call synchronises the host except
  *    attn_get_device_status.
  *  - Kernels launch as programmatic dependents of the kernel before them on
- *    the stream: they may become resident while it drains, but read no
- *    input and write no output before it has completed (the decode kernel
- *    only warms L2 with cache rows meanwhile).  Stream order is therefore
- *    unchanged for the caller, including for inputs that the previous
- *    kernel writes.
+ *    the stream: they may become resident while it drains, but no call reads
+ *    an input or writes an output before every kernel enqueued earlier on
+ *    the stream has completed (the decode kernel only warms L2 with cache
+ *    rows meanwhile).  Stream order is therefore unchanged for the caller,
+ *    including for inputs that the previous kernel writes.
  *  - Pointers and row strides must be 16-byte aligned (4 fp32 elements): the
  *    kernels move rows with 128-bit loads and TMA tiles.
  *  - A call with a rejected argument launches nothing and returns
