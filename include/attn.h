@@ -25,7 +25,10 @@
  *    an input or writes an output before every kernel enqueued earlier on
  *    the stream has completed (the decode kernel only warms L2 with cache
  *    rows meanwhile).  Stream order is therefore unchanged for the caller,
- *    including for inputs that the previous kernel writes.
+ *    including for inputs that the previous kernel writes.  (The guarantee
+ *    reaches past the previous kernel as long as every earlier kernel that
+ *    was itself launched as a programmatic dependent waits for its own
+ *    predecessor before completing, as all of this library's kernels do.)
  *  - Pointers and row strides must be 16-byte aligned (4 fp32 elements): the
  *    kernels move rows with 128-bit loads and TMA tiles.
  *  - A call with a rejected argument launches nothing and returns
