@@ -1,5 +1,6 @@
 """Host-side logic of bench.py (no GPU): multi-rank aggregation over gloo,
-clock-sample parsing, and the reference (oracle) arm's JSON line."""
+clock-sample parsing, the reference (oracle) arm's JSON line, and the hash
+that ties profiled DRAM traffic to the kernel code."""
 import json
 import os
 import subprocess
@@ -69,3 +70,13 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["metric"] == bench.METRIC
+
+
+def test_traffic_hash_ignores_comments_only():
+    """The counters in profiles/traffic.json stay attached to a kernel while
+    only its comments or blank space change, and drop when its code does."""
+    src = "int f(int x) {  // doubles x\n    return 2 * x; /* the\n  result */\n}\n"
+    same = "// header comment\nint f(int x) {\n  return 2 * x;\n}\n"
+    changed = "int f(int x) {  // doubles x\n    return 3 * x;\n}\n"
+    assert bench.code_text(src) == bench.code_text(same) == "int f(int x) { return 2 * x; }"
+    assert bench.code_text(changed) != bench.code_text(src)
