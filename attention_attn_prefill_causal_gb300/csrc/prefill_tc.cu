@@ -315,29 +315,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bool ok = true;
             for (int t = 0; t < kNQ && ok; ++t)
                 ok = mbar_wait(smem_u32(&bars.q_ready[t]), 0, wait_ns, status, kStatusTimeout);
+            // Descriptor bases, built once.  A descriptor keeps the start
+            // address as (address >> 4) in its low 14 bits, so an operand at
+            // byte offset off inside a tile is the tile's descriptor plus
+            // off >> 4 (shared-memory offsets stay below 256 KB: no carry).
+            // Each MMA below is then one 64-bit add away from issue: building
+            // descriptors between MMAs measured at less than half the MMA
+            // rate a single issuing thread reaches without it.
+            const uint64_t dq0 = smem_desc(sQ, 16, 1024, 2);
+            const uint64_t dq1 = smem_desc(sQ + L::kQTileBytes, 16, 1024, 2);
+            const uint64_t dk0 = smem_desc(sK, 16, 1024, 2);
+            const uint64_t dk1 = smem_desc(sK + L::kKTileBytes, 16, 1024, 2);
+            const uint64_t dv0 = smem_desc(sV, kBN * 128, 1024, 2);
+            const uint64_t dv1 = smem_desc(sV + L::kKTileBytes, kBN * 128, 1024, 2);
+            static_assert(kNQ == 2 && kStages == 2, "descriptor bases assume two tiles and two stages");
             auto issue_s = [&](int t, uint32_t j) {
-                const uint32_t st = j % kStages;
-                const uint32_t qa = sQ + t * L::kQTileBytes, kb = sK + st * L::kKTileBytes;
+                const uint64_t a0 = t == 0 ? dq0 : dq1;
+                const uint64_t b0 = (j % kStages) == 0 ? dk0 : dk1;
+                const uint32_t d = tmem + t * 256;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
-                    const uint32_t offk = (ks / 4) * (kBN * 128) + (ks % 4) * 32;
-                    mma_f16_ss(tmem + t * 256, smem_desc(qa + off, 16, 1024, 2),
-                               smem_desc(kb + offk, 16, 1024, 2), idesc_s, ks > 0);
+                    const uint64_t offa = (uint64_t)((ks / 4) * (kBM * 128 / 16) + (ks % 4) * 2);
+                    const uint64_t offb = (uint64_t)((ks / 4) * (kBN * 128 / 16) + (ks % 4) * 2);
+                    mma_f16_ss(d, a0 + offa, b0 + offb, idesc_s, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(smem_u32(&bars.s_full[t]));
             };
             auto issue_pv = [&](int t, uint32_t j) {
-                const uint32_t st = j % kStages;
-                const uint32_t vb = sV + st * L::kKTileBytes;
+                // V tile is MN-major: 64-column boxes are kBN*128 bytes apart
+                // (leading byte offset), 8-key groups 1024 bytes apart (stride);
+                // K-step ks starts 16 keys (2048 bytes) further on.
+                const uint64_t b0 = (j % kStages) == 0 ? dv0 : dv1;
+                const uint32_t d = tmem + t * 256 + 128, a = tmem + t * 256;
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks) {
-                    // V tile is MN-major: 64-column boxes are kBN*128 bytes apart
-                    // (leading byte offset), 8-key groups 1024 bytes apart (stride).
-                    mma_f16_ts(tmem + t * 256 + 128, tmem + t * 256 + ks * 8,
-                               smem_desc(vb + ks * 2048, kBN * 128, 1024, 2), idesc_pv,
-                               (j > 0 || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    mma_f16_ts(d, a + ks * 8, b0 + (uint64_t)(ks * (2048 / 16)), idesc_pv,
+                               ks > 0 ? 1u : acc0);
             };
             if (ok && n_kv_all > 0) {
                 ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, wait_ns, status, kStatusTimeout);
