@@ -615,7 +615,9 @@ def bench_layer_stack(attn, shape, device, stream, layers=28, reps=5):
     g = make_graph(one_pass, stream)
     graph_ms, graph_host_ms = timed(g.replay)
     return {"workload": f"{layers} layers x {shape.name}", "layers": layers,
-            "launches_per_pass": 2 * layers,
+            # per layer: rounding pre-pass, main kernel, and the combine of the
+            # split key walk (this workload splits it)
+            "launches_per_pass": 3 * layers,
             "eager_ms_per_pass": round(eager_ms, 4), "graph_ms_per_pass": round(graph_ms, 4),
             "eager_host_ms_per_pass": round(eager_host_ms, 4),
             "graph_host_ms_per_pass": round(graph_host_ms, 4)}
