@@ -329,6 +329,12 @@ class PrefillBench:
         ws = attn.attn_prefill_workspace_size(shape.m, shape.num_q_heads, shape.num_kv_heads,
                                               shape.head_dim, attn.ATTN_PREC_FP16)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        # The workspace holds the rounded K and V (two 256-byte aligned fp16
+        # matrices) and, when the call splits its key walk, the partials that
+        # a third kernel merges.
+        kv_bytes = shape.m * shape.num_kv_heads * shape.head_dim * 2
+        operands = 2 * ((kv_bytes + 255) // 256 * 256)
+        self.launches_per_call = 3 if ws > operands else 2
 
     def call(self, i, stream):
         c, a, r = self.c, self.attn, i % self.R
@@ -485,7 +491,7 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
                 "ms_per_call": round(e2e_per_call * 1e3, 4),
                 "serial": {"value": round(flops / serial_per_call / 1e12, 2),
                            "ms_per_call": round(serial_per_call * 1e3, 4)}},
-        "gpu_launches_per_call": 2,
+        "gpu_launches_per_call": pb.launches_per_call,
     }
 
 
