@@ -32,6 +32,9 @@
 // may overwrite the TMEM that held P_t(j) right after PV_t(j) is issued, and
 // the commit that signals S_t(j+1) also covers PV_t(j): once softmax t sees
 // S_t(j+1) its O accumulator is stable and can be rescaled.
+// The MMA thread builds each operand tile's descriptor once and reaches the
+// operand of every K step with one 64-bit add: work between consecutive MMAs
+// on the issuing thread directly lowers the rate the tensor pipe is fed at.
 // Rescaling is conditional: the running max used for the exponentials only
 // moves when the row max grows by more than 8 (log2 units); the final O / l
 // is exact either way, and P stays below 2^8.
@@ -39,6 +42,13 @@
 // thread writes its row of O into 128-byte swizzled staging boxes there, and
 // one thread per tile stores them with TMA tensor stores, so O leaves in
 // whole 128-byte lines rather than one 16-byte piece per row and instruction.
+// Small grids (query-tile pairs x heads below the SM count) split each
+// pair's key walk into chunks of C tiles, one work item per chunk; chunks
+// write unnormalised partials and a combine kernel merges them.
+// Launch chain: the rounding pre-pass waits for the kernel before the call
+// and then lets this kernel launch; this kernel stages the caller's fp32 Q at
+// once and waits for the pre-pass only before its first K tile; the combine
+// waits for this kernel (all programmatic dependent launches).
 // Every mbarrier wait is bounded; on a timeout a thread records
 // kStatusTimeout in the device status word, abandons its loop, and the CTA
 // still drains its copies, waits for its MMAs and frees TMEM before exiting.
