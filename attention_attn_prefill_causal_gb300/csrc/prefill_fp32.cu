@@ -43,9 +43,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int D, int kBM>
 struct Smem {
     static constexpr int kPitch = D + 4;  // pad: 128-bit reads across rows hit distinct banks
+    // The weights of a tile ([kBM][kBN] floats) are staged over the K tile
+    // once every warp's dot products are done, when they fit there; else
+    // (head_dim 32 with 64-row blocks) in an array of their own.
+    static constexpr bool kPInK = kBN * kPitch >= kBM * kBN;
     float q[kBM][kPitch];
     float k[kBN][kPitch];
     float v[kBN][D];
+    float p[kPInK ? 4 : kBM * kBN];
 };
 
 template <int D>
@@ -117,8 +122,9 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     const uint32_t n_tiles = last_row / kBN + 1;
 
     // This warp's weights for the current tile, [kRowsPerWarp][kBN], staged
-    // over the K tile once every warp has finished its dot products.
-    float* const sp = &sm.k[0][0] + wr0 * kBN;
+    // over the K tile once every warp has finished its dot products (or in
+    // their own array when the K tile is too small).
+    float* const sp = (Smem<D, kBM>::kPInK ? &sm.k[0][0] : &sm.p[0]) + wr0 * kBN;
     for (uint32_t t = 0; t < n_tiles; ++t) {
         const uint32_t k0 = t * kBN;
         __syncthreads();  // the previous tile's P.V no longer reads K (P) or V

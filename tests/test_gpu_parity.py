@@ -155,11 +155,13 @@ def test_prefill_fp32_small_head_dims(attn, d):
     _check_prefill(attn, 200, 6, 2, d, FP32, seed=d)
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("m,hq,hkv", [(1000, 40, 8), (77, 40, 8), (1000, 2, 1)])
-def test_prefill_fp32_both_query_block_sizes(attn, m, hq, hkv):
+def test_prefill_fp32_both_query_block_sizes(attn, m, hq, hkv, d):
     """The fp32 kernel takes 64-row query blocks when they fill the SMs twice
-    over (the first case) and 16-row blocks otherwise; ragged tails in both."""
-    _check_prefill(attn, m, hq, hkv, 64, FP32, seed=m + hq)
+    over (the first case) and 16-row blocks otherwise; ragged tails in both,
+    at every head_dim (the shared-memory layout of the weights differs)."""
+    _check_prefill(attn, m, hq, hkv, d, FP32, seed=m + hq + d)
 
 
 def test_prefill_long_sequence_sampled_rows(attn):
