@@ -66,6 +66,46 @@ def _decode_cases(n=32, seed=20261204):
     return cases
 
 
+def _wide_prefill_cases(n=32, seed=99101):
+    """Longer prompts (up to 6000 tokens, up to 32 query heads): more split
+    plans and grids of several waves."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        prec = int(rng.choice([FP32, FP16, FP16, FP16, BF16]))
+        d = int(rng.choice([64, 128])) if prec != FP32 else int(rng.choice([32, 64, 128]))
+        hkv = int(rng.choice([1, 2, 4, 8]))
+        g = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8]))
+        while hkv * g > 32:
+            g //= 2
+        m = int(rng.integers(1, 6001)) if prec != FP32 else int(rng.integers(1, 3001))
+        cases.append((100 + i, prec, m, hkv * g, hkv, d, 4 * int(rng.integers(0, 9)),
+                      4 * int(rng.integers(0, 9)), float(rng.choice([0.5, 1.0])),
+                      float(rng.choice([0.0, 0.0, 0.05])), m > 1200))
+    return cases
+
+
+def _wide_decode_cases(n=32, seed=99102):
+    """Caches up to 100000 rows and GQA groups up to 16 (several warp steps,
+    the one-step-ahead L2 prefetch, ragged tails)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        hkv = int(rng.choice([1, 2, 3, 4, 8]))
+        g = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16]))
+        while hkv * g > 64:
+            g //= 2
+        d = int(rng.choice([32, 64, 128]))
+        S = int(rng.integers(1, 100001))
+        T = int(rng.integers(1, S + 1))
+        W = 0 if rng.random() < 0.5 else int(rng.integers(1, T + 100))
+        fused = bool(rng.random() < 0.5)
+        rope = fused and bool(rng.random() < 0.5)
+        cases.append((100 + i, hkv * g, hkv, d, S, T, W, fused, rope,
+                      float(rng.choice([0.0, 0.02]))))
+    return cases
+
+
 @pytest.fixture(scope="module")
 def attn():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
@@ -74,7 +114,7 @@ def attn():
     return a
 
 
-@pytest.mark.parametrize("case", _prefill_cases(), ids=lambda c: f"p{c[0]}")
+@pytest.mark.parametrize("case", _prefill_cases() + _wide_prefill_cases(), ids=lambda c: f"p{c[0]}")
 def test_fuzz_prefill(attn, case):
     i, prec, m, hq, hkv, d, q_pad, kv_pad, mul, scale, big = case
     qs, kvs = hq * d + q_pad, hkv * d + kv_pad
@@ -104,7 +144,7 @@ def _rope_tables(d, seed):
     return np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
 
 
-@pytest.mark.parametrize("case", _decode_cases(), ids=lambda c: f"d{c[0]}")
+@pytest.mark.parametrize("case", _decode_cases() + _wide_decode_cases(), ids=lambda c: f"d{c[0]}")
 def test_fuzz_decode(attn, case):
     i, hq, hkv, d, S, T, W, fused, rope, scale = case
     q, kc, vc, kn, vn = workloads.decode_inputs(hq, hkv, d, S, seed=3000 + i, append=True)
