@@ -22,6 +22,17 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // bounded device waits give
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// True for page-locked host memory the device addresses directly.
+bool in_host_memory(const void* p) {
+    if (!p) return false;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not a pointer CUDA knows: not staged
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+
 uint64_t wait_limit_ns() {
     static uint64_t v = []() -> uint64_t {
         const char* e = std::getenv("ATTN_WAIT_LIMIT_US");
@@ -199,6 +210,7 @@ attn_status_t attn_decode(const float* q, const float* k_cache, const float* v_c
     c.max_seq = max_seq;
     c.total_seq = total_seq;
     c.scale = resolve_scale(scale, head_dim);
+    c.stage_inputs = in_host_memory(q);
     return record_cuda_error(
         launch_decode(c, plan, workspace, static_cast<cudaStream_t>(stream)));
 }
@@ -237,6 +249,8 @@ attn_status_t attn_decode_append(const float* q, const float* k_new, const float
     c.total_seq = total_seq;
     c.position = position;
     c.scale = resolve_scale(scale, head_dim);
+    c.stage_inputs = in_host_memory(q) || in_host_memory(k_new) || in_host_memory(v_new) ||
+                     in_host_memory(rope_cos) || in_host_memory(rope_sin);
     return record_cuda_error(
         launch_decode(c, plan, workspace, static_cast<cudaStream_t>(stream)));
 }

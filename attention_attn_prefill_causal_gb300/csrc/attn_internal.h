@@ -55,6 +55,7 @@ struct DecodePlan {
     uint32_t n_splits;        // CTAs (row chunks) per KV head group
     size_t part_o_floats;
     size_t part_ml_floats;
+    size_t stage_floats;      // copies of q, k_new, v_new and the RoPE tables
     size_t workspace_bytes;
 };
 DecodePlan make_decode_plan(uint32_t num_heads, uint32_t kv_heads, uint32_t head_dim,
@@ -74,6 +75,10 @@ struct DecodeCall {
     float* out;
     uint32_t num_heads, kv_heads, head_dim, max_seq, total_seq, position;
     float scale;
+    // Some step input (q, k_new, v_new, RoPE tables) is in page-locked host
+    // memory: copy them into the workspace once, so that the decode CTAs
+    // read them from HBM instead of each reading them over the host link.
+    bool stage_inputs;
 };
 
 cudaError_t launch_decode(const DecodeCall& call, const DecodePlan& plan, void* workspace,

@@ -589,6 +589,40 @@ __global__ void __launch_bounds__(512) decode_combine_kernel(const CombineArgs a
     }
 }
 
+// Copies a decode step's small inputs (q, k_new, v_new: float4 counts n_q,
+// n_kv, n_kv; the RoPE tables: n_half floats each, read as floats since the
+// caller's tables need only 4-byte alignment) into the workspace, when
+// some of them sit in page-locked host memory: one CTA reads them over the
+// host link once, and the decode CTAs then read the copies from HBM.  A
+// programmatic dependent of the kernel before it; the decode kernel is one of
+// it (it may start its L2 prefetch of the cache at once and waits for this
+// grid before reading any input).
+__global__ void __launch_bounds__(256) stage_step_inputs_kernel(
+    const float4* __restrict__ q, const float4* __restrict__ k_new,
+    const float4* __restrict__ v_new, const float* __restrict__ rope_cos,
+    const float* __restrict__ rope_sin, float4* __restrict__ dst, uint32_t n_q, uint32_t n_kv,
+    uint32_t n_half) {
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (uint32_t i = threadIdx.x; i < n_q; i += blockDim.x) dst[i] = q[i];
+    float4* dk = dst + n_q;
+    float4* dv = dk + n_kv;
+    if (k_new) {
+        for (uint32_t i = threadIdx.x; i < n_kv; i += blockDim.x) {
+            dk[i] = k_new[i];
+            dv[i] = v_new[i];
+        }
+    }
+    float* dc = reinterpret_cast<float*>(dv + n_kv);
+    float* dsn = dc + n_half;
+    if (rope_cos) {
+        for (uint32_t i = threadIdx.x; i < n_half; i += blockDim.x) {
+            dc[i] = rope_cos[i];
+            dsn[i] = rope_sin[i];
+        }
+    }
+}
+
 __global__ void kv_append_kernel(const float4* __restrict__ k_src, const float4* __restrict__ v_src,
                                  float4* __restrict__ k_cache, float4* __restrict__ v_cache,
                                  uint32_t kv_heads, uint32_t d4, uint32_t max_seq,
@@ -686,8 +720,10 @@ DecodePlan make_decode_plan(uint32_t num_heads, uint32_t kv_heads, uint32_t head
     p.n_splits = p.rows_live ? (p.rows_live + chunk - 1) / chunk : 0;
     p.part_o_floats = (size_t)num_heads * p.n_splits * head_dim;
     p.part_ml_floats = (size_t)num_heads * p.n_splits * 2;
+    p.stage_floats = (size_t)(num_heads + 2 * kv_heads + 1) * head_dim;
     p.workspace_bytes = (p.part_o_floats * 4 + 255) / 256 * 256 +
-                        (p.part_ml_floats * 4 + 255) / 256 * 256;
+                        (p.part_ml_floats * 4 + 255) / 256 * 256 +
+                        (p.stage_floats * 4 + 255) / 256 * 256;
     return p;
 }
 
@@ -717,6 +753,40 @@ cudaError_t launch_decode(const DecodeCall& c, const DecodePlan& plan, void* wor
     a.n_splits = plan.n_splits;
     a.position = c.k_new ? c.position : kNoRow;
     a.scale_log2 = c.scale * kLog2e;
+    if (c.stage_inputs) {
+        // Stage the step inputs into the workspace (after the partials), then
+        // point the decode at the copies.
+        float* st = reinterpret_cast<float*>(ws + (plan.part_o_floats * 4 + 255) / 256 * 256 +
+                                             (plan.part_ml_floats * 4 + 255) / 256 * 256);
+        const uint32_t n_q = c.num_heads * c.head_dim / 4, n_kv = c.kv_heads * c.head_dim / 4;
+        const uint32_t n_half = c.head_dim / 2;  // cos and sin: head_dim/2 floats each
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(
+            &cfg, stage_step_inputs_kernel, reinterpret_cast<const float4*>(c.q),
+            reinterpret_cast<const float4*>(c.k_new), reinterpret_cast<const float4*>(c.v_new),
+            c.rope_cos, c.rope_sin, reinterpret_cast<float4*>(st), n_q, n_kv, n_half);
+        if (e != cudaSuccess) return e;
+        a.q = st;
+        float* sk = st + (size_t)n_q * 4;
+        float* sv = sk + (size_t)n_kv * 4;
+        float* sc = sv + (size_t)n_kv * 4;
+        if (c.k_new) {
+            a.k_new = sk;
+            a.v_new = sv;
+        }
+        if (c.rope_cos) {
+            a.rope_cos = sc;
+            a.rope_sin = sc + n_half;
+        }
+    }
     switch (c.head_dim) {
         case 32: return launch_d<32>(a, plan, c.kv_heads, c.num_heads, stream);
         case 64: return launch_d<64>(a, plan, c.kv_heads, c.num_heads, stream);
@@ -748,7 +818,8 @@ cudaError_t launch_kv_append(const float* k_src, const float* v_src, float* k_ca
 // its own pools (a KV-cache pool that owns every free byte), a plugin
 // interface that passes only input and output pointers, or a latency-bound
 // loop that forbids allocation and the implicit synchronisation it can bring.
-// For them the decode workspace (the per-chunk partial results) lives in one
+// For them the decode workspace (the per-chunk partial results, and copies
+// of host-resident step inputs) lives in one
 // file-scope device array of kNoAllocScratchBytes.  Every GPU that loads
 // this library keeps that array resident until the process exits.  The array
 // is shared by every call on a device and keeps the last call's contents;

@@ -13,7 +13,9 @@
  *    addresses directly (cudaHostAlloc / cudaMallocHost under unified
  *    addressing, or cudaHostRegister with cudaHostRegisterMapped).  The
  *    kernels then read and write those bytes over the CPU-GPU link in the
- *    call itself, with no separate copy.  Caches, workspaces and every
+ *    call itself, with no separate copy (a decode call whose inputs are
+ *    host-resident first copies them into its workspace with one small
+ *    kernel, so that every CTA then reads them from HBM).  Caches, workspaces and every
  *    prefill buffer must be device memory (they are moved with TMA and bulk
  *    copies).  Pageable host memory is not supported anywhere.
  *  - Every compute call is asynchronous on `stream` (a cudaStream_t passed as
