@@ -794,8 +794,9 @@ def our_arm(args):
     # v_new from page-locked host memory and leaves its output in page-locked
     # host memory.  Two transports, each timed as eager Python calls and as
     # CUDA-graph replays of R steps:
-    #  * host-resident: the call gets the host buffers; its kernels read the
-    #    inputs and write the output over the CPU-GPU link (no memcpy);
+    #  * host-resident: the call gets the host buffers; a one-CTA kernel of
+    #    the call copies the inputs into the workspace over the CPU-GPU link
+    #    and the combine writes the output there (no memcpy);
     #  * memcpy: one H2D copy of the packed inputs, the call on device
     #    buffers, one D2H copy of the output.
     # `value` is the eager host-resident step (max over ranks): one Python
@@ -926,9 +927,10 @@ def our_arm(args):
                     "h2d_bytes_per_step": (q.numel() + kn.numel() + vn.numel()) * 4,
                     "d2h_bytes_per_step": shape.num_heads * shape.head_dim * 4,
                     "method": "one attn_decode_append Python call per step with q, k_new, "
-                              "v_new and out in page-locked host memory (the kernels read and "
-                              "write them over the CPU-GPU link each step); the K/V caches stay "
-                              "resident in HBM (decode state)",
+                              "v_new and out in page-locked host memory: the call copies the "
+                              "inputs into its workspace with one small kernel and writes out "
+                              "over the CPU-GPU link, no memcpy; the K/V caches stay resident "
+                              "in HBM (decode state)",
                     "variants": e_variants},
             "gpu_launches": args.steps * db.launches_per_step,
             "clocks": clocks,
