@@ -597,29 +597,48 @@ __global__ void __launch_bounds__(512) decode_combine_kernel(const CombineArgs a
 // programmatic dependent of the kernel before it; the decode kernel is one of
 // it (it may start its L2 prefetch of the cache at once and waits for this
 // grid before reading any input).
-__global__ void __launch_bounds__(256) stage_step_inputs_kernel(
+__global__ void __launch_bounds__(512) stage_step_inputs_kernel(
     const float4* __restrict__ q, const float4* __restrict__ k_new,
     const float4* __restrict__ v_new, const float* __restrict__ rope_cos,
     const float* __restrict__ rope_sin, float4* __restrict__ dst, uint32_t n_q, uint32_t n_kv,
     uint32_t n_half) {
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (uint32_t i = threadIdx.x; i < n_q; i += blockDim.x) dst[i] = q[i];
-    float4* dk = dst + n_q;
-    float4* dv = dk + n_kv;
-    if (k_new) {
-        for (uint32_t i = threadIdx.x; i < n_kv; i += blockDim.x) {
-            dk[i] = k_new[i];
-            dv[i] = v_new[i];
-        }
+    // One flat index over q, k_new, v_new (float4s): every load of a thread is
+    // issued before any store, so the copy costs one host-link round trip
+    // for up to 4 x 512 float4s (32 KB).
+    const uint32_t n_kv_all = k_new ? n_kv : 0u;
+    const uint32_t total = n_q + 2 * n_kv_all;
+    constexpr int kPer = 4;
+    float4 x[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const uint32_t i = threadIdx.x + u * blockDim.x;
+        if (i < n_q) x[u] = q[i];
+        else if (i < n_q + n_kv_all) x[u] = k_new[i - n_q];
+        else if (i < total) x[u] = v_new[i - n_q - n_kv_all];
     }
-    float* dc = reinterpret_cast<float*>(dv + n_kv);
-    float* dsn = dc + n_half;
-    if (rope_cos) {
-        for (uint32_t i = threadIdx.x; i < n_half; i += blockDim.x) {
-            dc[i] = rope_cos[i];
-            dsn[i] = rope_sin[i];
-        }
+    float cs = 0.f, sn = 0.f;
+    const bool rope_here = rope_cos && threadIdx.x < n_half;
+    if (rope_here) {
+        cs = rope_cos[threadIdx.x];
+        sn = rope_sin[threadIdx.x];
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const uint32_t i = threadIdx.x + u * blockDim.x;
+        if (i < total) dst[i] = x[u];
+    }
+    // the rest, should the inputs exceed one pass (more than 32 KB)
+    for (uint32_t i = threadIdx.x + kPer * blockDim.x; i < total; i += blockDim.x) {
+        if (i < n_q) dst[i] = q[i];
+        else if (i < n_q + n_kv_all) dst[i] = k_new[i - n_q];
+        else dst[i] = v_new[i - n_q - n_kv_all];
+    }
+    float* dc = reinterpret_cast<float*>(dst + n_q + 2 * n_kv);
+    if (rope_here) {
+        dc[threadIdx.x] = cs;
+        dc[n_half + threadIdx.x] = sn;
     }
 }
 
@@ -765,7 +784,7 @@ cudaError_t launch_decode(const DecodeCall& c, const DecodePlan& plan, void* wor
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, 1);
-        cfg.blockDim = dim3(256, 1, 1);
+        cfg.blockDim = dim3(512, 1, 1);
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
