@@ -131,3 +131,16 @@ def test_kv_append_rejects_bad_arguments(attn, kw, expect):
     st = attn.lib.kv_append(a["k_src"], a["v_src"], a["k_cache"], a["v_cache"], a["kv_heads"],
                             a["head_dim"], a["max_seq"], a["position"], None)
     assert st == expect
+
+
+@pytest.mark.parametrize("hq,hkv,d,T,W", [(12, 2, 128, 4096, 0), (32, 8, 128, 32768, 4096),
+                                          (4, 1, 32, 1, 0), (64, 8, 64, 100000, 0)])
+def test_decode_workspace_has_room_for_staged_inputs(attn, hq, hkv, d, T, W):
+    """A decode call with host-resident step inputs copies q, k_new, v_new and
+    the RoPE tables ((hq + 2 hkv + 1) * head_dim floats) into its workspace,
+    after the partials (one (max, sum) pair and head_dim floats per query head
+    and chunk): the size covers both, whatever the chunk count."""
+    ws = attn.attn_decode_workspace_size(hq, hkv, d, T, W)
+    stage = (hq + 2 * hkv + 1) * d * 4
+    assert ws >= stage + hq * (d + 2) * 4
+    assert ws % 256 == 0
