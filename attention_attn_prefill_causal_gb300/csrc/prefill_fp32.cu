@@ -9,14 +9,15 @@
 //
 // The page runs one warp per query head, walking all M rows serially and
 // reading K/V through L2.  Here a CTA takes a block of query rows of one
-// head (64 rows, or 16 when the problem is too small to fill the SMs with
-// 64-row blocks) and walks 64-key tiles staged in shared memory, so each K/V
-// row is read from global memory once per block instead of once per row:
-//  * a warp owns 8 (or 2) query rows and scores all of them at once, each
+// head (64, 32 or 16 rows: the largest size that still gives every SM
+// several blocks) and walks 64-key tiles staged in shared memory, so each
+// K/V row is read from global memory once per block instead of once per row:
+//  * tiles arrive by asynchronous 16-byte copies (cp.async), K and V in
+//    separate groups: the scores wait for K only, so V lands during them;
+//  * a warp owns 8, 4 or 2 query rows and scores all of them at once, each
 //    lane taking keys lane and lane + 32 of the tile (dot products over
 //    head_dim from shared memory: two 128-bit K reads per lane feed every
-//    row, the Q reads are broadcasts), so each shared-memory wavefront
-//    feeds about 128 FMAs;
+//    row, the Q reads are broadcasts);
 //  * per row, the tile's max and sum come from warp shuffles; the online
 //    softmax runs in base 2 (scores pre-multiplied by log2 e, as the page
 //    does before ex2);
@@ -24,6 +25,8 @@
 //    (free once every warp's dot products are done); each lane owns
 //    head_dim/32 output elements and reads four keys' weights of a row with
 //    one broadcast 128-bit load, stopping at the warp's last attended key.
+// The grid runs heads fastest and query blocks longest causal extent first,
+// so the longest walks of every head start in the first wave.
 // Causal masking is the loop bound plus a per-key test on the diagonal tile.
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -53,36 +56,37 @@ struct Smem {
     float p[kPInK ? 4 : kBM * kBN];
 };
 
-template <int D>
-__device__ __forceinline__ void load_tile(float (*dst)[D + 4], const float* __restrict__ src,
-                                          uint32_t row0, uint32_t m, uint32_t stride,
-                                          uint32_t col0, int rows) {
+// Asynchronous 16-byte copies of `rows` rows of D floats (from column col0 of
+// rows row0, row0 + 1, ... of a matrix with row pitch `stride`) into shared
+// memory with row pitch PITCH floats.  Rows at or past m are zero-filled: the
+// copy reads 0 source bytes, from row 0 so that the address stays valid.
+template <int D, int PITCH>
+__device__ __forceinline__ void copy_rows_async(float* dst, const float* __restrict__ src,
+                                                uint32_t row0, uint32_t m, uint32_t stride,
+                                                uint32_t col0, int rows) {
     constexpr int C4 = D / 4;
+#pragma unroll 4
     for (int t = threadIdx.x; t < rows * C4; t += kThreads) {
         const int r = t / C4, c = (t % C4) * 4;
-        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row0 + r < m)
-            val = *reinterpret_cast<const float4*>(src + (size_t)(row0 + r) * stride + col0 + c);
-        *reinterpret_cast<float4*>(&dst[r][c]) = val;
+        const bool live = row0 + r < m;
+        const float* g = src + (size_t)(live ? row0 + r : 0u) * stride + col0 + c;
+        const uint32_t sa = (uint32_t)__cvta_generic_to_shared(dst + r * PITCH + c);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                     :: "r"(sa), "l"(g), "r"(live ? 16u : 0u) : "memory");
     }
 }
-
-template <int D>
-__device__ __forceinline__ void load_v_tile(float (*dst)[D], const float* __restrict__ src,
-                                            uint32_t row0, uint32_t m, uint32_t stride,
-                                            uint32_t col0) {
-    constexpr int C4 = D / 4;
-    for (int t = threadIdx.x; t < kBN * C4; t += kThreads) {
-        const int r = t / C4, c = (t % C4) * 4;
-        float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row0 + r < m)
-            val = *reinterpret_cast<const float4*>(src + (size_t)(row0 + r) * stride + col0 + c);
-        *reinterpret_cast<float4*>(&dst[r][c]) = val;
-    }
+__device__ __forceinline__ void copies_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void copies_wait() {
+    asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
 }
 
-// kBM query rows per CTA (64 for large problems; 16 when 64-row blocks
-// would leave most SMs idle, which also shortens each warp's serial chain).
+// kBM query rows per CTA (64 for large problems; 32 or 16 when fewer blocks
+// would leave the longest causal walks alone on a few SMs).  Grid: x = query
+// head, y (+ z * gridDim.y) = query block counted from the last.
 template <int D, int kBM>
 __global__ void __launch_bounds__(kThreads, 2)
 prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
@@ -96,8 +100,10 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t nqb = (m + kBM - 1) / kBM;
-    const uint32_t qb = nqb - 1 - blockIdx.x;  // longest causal extent first
-    const uint32_t h = blockIdx.y;
+    const uint32_t qb_rev = blockIdx.z * gridDim.y + blockIdx.y;
+    if (qb_rev >= nqb) return;                 // past the last block (z overhang)
+    const uint32_t qb = nqb - 1 - qb_rev;      // longest causal extent first
+    const uint32_t h = blockIdx.x;
     const uint32_t kvh = h / heads_per_kv;
     const uint32_t q0 = qb * kBM;
 
@@ -106,7 +112,8 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     // global read and write comes after the grid dependency resolves.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    load_tile<D>(sm.q, q, q0, m, q_stride, h * D, kBM);
+    copy_rows_async<D, D + 4>(&sm.q[0][0], q, q0, m, q_stride, h * D, kBM);
+    copies_commit();
 
     float mrow[kRowsPerWarp], lrow[kRowsPerWarp], acc[kRowsPerWarp][VEC];
 #pragma unroll
@@ -128,8 +135,11 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
     for (uint32_t t = 0; t < n_tiles; ++t) {
         const uint32_t k0 = t * kBN;
         __syncthreads();  // the previous tile's P.V no longer reads K (P) or V
-        load_tile<D>(sm.k, k, k0, m, kv_stride, kvh * D, kBN);
-        load_v_tile<D>(sm.v, v, k0, m, kv_stride, kvh * D);
+        copy_rows_async<D, D + 4>(&sm.k[0][0], k, k0, m, kv_stride, kvh * D, kBN);
+        copies_commit();
+        copy_rows_async<D, D>(&sm.v[0][0], v, k0, m, kv_stride, kvh * D, kBN);
+        copies_commit();
+        copies_wait<1>();  // Q and this tile's K have landed (V may still be in flight)
         __syncthreads();
         const bool active = k0 <= wrow_last;  // some key of the tile is attended by the warp
         // ---- scores: lane holds keys kA = k0 + lane and kB = k0 + 32 + lane
@@ -184,7 +194,8 @@ prefill_fp32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                 sB[r] = pb;
             }
         }
-        __syncthreads();  // every warp's dot products are done: the K tile is free
+        copies_wait<0>();  // this tile's V has landed
+        __syncthreads();  // every warp's dot products are done (the K tile is free); V is visible
         if (!active) continue;
         // ---- O += P V.  The weights go to shared memory (row r, key j at
         // sp[r * kBN + j]); each lane then reads four keys' weights of a row
@@ -257,7 +268,9 @@ cudaError_t launch_bm(const float* q, const float* k, const float* v, float* o, 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((m + BM - 1) / BM, num_q_heads, 1);
+    const uint32_t nqb = (m + BM - 1) / BM;
+    const uint32_t gy = nqb < 65535u ? nqb : 65535u;
+    cfg.gridDim = dim3(num_q_heads, gy, (nqb + gy - 1) / gy);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
@@ -271,10 +284,17 @@ template <int D>
 cudaError_t launch_d(const float* q, const float* k, const float* v, float* o, uint32_t m,
                      uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
                      uint32_t kv_stride, float scale, cudaStream_t stream) {
-    // 64-row blocks when they give at least two CTAs per SM, else 16-row blocks.
+    // The largest block that still gives the SMs several blocks each: 64
+    // rows from four 64-row blocks per SM, 32 rows from one, else 16 rows.
+    // Larger blocks read each K/V tile for more rows; smaller ones shorten
+    // the longest causal walk, which bounds the call when blocks are few.
     const uint64_t blocks64 = (uint64_t)((m + 63) / 64) * num_q_heads;
-    if (blocks64 >= 2ull * (uint64_t)device_sm_count())
+    const uint64_t sms = (uint64_t)device_sm_count();
+    if (blocks64 >= 4 * sms)
         return launch_bm<D, 64>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
+                                scale, stream);
+    if (blocks64 >= sms)
+        return launch_bm<D, 32>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
                                 scale, stream);
     return launch_bm<D, 16>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride, scale,
                             stream);

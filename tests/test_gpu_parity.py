@@ -156,11 +156,13 @@ def test_prefill_fp32_small_head_dims(attn, d):
 
 
 @pytest.mark.parametrize("d", [32, 64, 128])
-@pytest.mark.parametrize("m,hq,hkv", [(1000, 40, 8), (77, 40, 8), (1000, 2, 1)])
-def test_prefill_fp32_both_query_block_sizes(attn, m, hq, hkv, d):
-    """The fp32 kernel takes 64-row query blocks when they fill the SMs twice
-    over (the first case) and 16-row blocks otherwise; ragged tails in both,
-    at every head_dim (the shared-memory layout of the weights differs)."""
+@pytest.mark.parametrize("m,hq,hkv", [(1000, 40, 8), (1000, 12, 2), (77, 40, 8), (1000, 2, 1)])
+def test_prefill_fp32_every_query_block_size(attn, m, hq, hkv, d):
+    """The fp32 kernel takes 64-row query blocks when there are at least four
+    64-row blocks per SM (640 blocks here, the first case), 32-row blocks
+    from one per SM (192, the second) and 16-row blocks below that (the last
+    two); ragged tails in each, at every head_dim (the shared-memory layout
+    of the weights differs)."""
     _check_prefill(attn, m, hq, hkv, d, FP32, seed=m + hq + d)
 
 
