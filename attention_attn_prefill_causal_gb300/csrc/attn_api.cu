@@ -90,6 +90,23 @@ void set_last_error(const char* msg) {
     std::snprintf(t_last_error, sizeof(t_last_error), "%s", msg);
 }
 
+// Validation of the decode arguments other than the workspace, shared by
+// every decode entry point.
+attn_status_t check_decode_args(const float* q, const float* k_cache, const float* v_cache,
+                                const float* out, uint32_t num_heads, uint32_t kv_heads,
+                                uint32_t head_dim, uint32_t max_seq, uint32_t total_seq,
+                                float scale) {
+    if (!q || !k_cache || !v_cache || !out) return ATTN_ERR_INVALID_ARG;
+    if (num_heads == 0 || kv_heads == 0 || num_heads % kv_heads != 0) return ATTN_ERR_INVALID_ARG;
+    if (head_dim == 0 || head_dim % 32 != 0) return ATTN_ERR_INVALID_ARG;
+    if (total_seq == 0 || total_seq > max_seq) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return ATTN_ERR_INVALID_ARG;
+    if (!(scale >= 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (head_dim != 32 && head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
 }  // namespace attn
 
 using namespace attn;
@@ -170,20 +187,16 @@ size_t attn_decode_workspace_size(uint32_t num_heads, uint32_t kv_heads, uint32_
         .workspace_bytes;
 }
 
+
 // Shared validation of the decode entry points; fills the plan.
 static attn_status_t check_decode(const float* q, const float* k_cache, const float* v_cache,
                                   const float* out, uint32_t num_heads, uint32_t kv_heads,
                                   uint32_t head_dim, uint32_t max_seq, uint32_t total_seq,
                                   uint32_t window, float scale, const void* workspace,
                                   size_t workspace_bytes, DecodePlan* plan) {
-    if (!q || !k_cache || !v_cache || !out) return ATTN_ERR_INVALID_ARG;
-    if (num_heads == 0 || kv_heads == 0 || num_heads % kv_heads != 0) return ATTN_ERR_INVALID_ARG;
-    if (head_dim == 0 || head_dim % 32 != 0) return ATTN_ERR_INVALID_ARG;
-    if (total_seq == 0 || total_seq > max_seq) return ATTN_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-        return ATTN_ERR_INVALID_ARG;
-    if (!(scale >= 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
-    if (head_dim != 32 && head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    const attn_status_t st = check_decode_args(q, k_cache, v_cache, out, num_heads, kv_heads,
+                                               head_dim, max_seq, total_seq, scale);
+    if (st != ATTN_OK) return st;
     *plan = make_decode_plan(num_heads, kv_heads, head_dim, total_seq, window, device_sm_count());
     if (!workspace || workspace_bytes < plan->workspace_bytes) return ATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;

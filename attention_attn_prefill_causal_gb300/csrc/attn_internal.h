@@ -81,6 +81,13 @@ struct DecodeCall {
     bool stage_inputs;
 };
 
+// Validation of the decode arguments other than the workspace (null and
+// misaligned pointers, head counts, head_dim, total_seq, scale).
+attn_status_t check_decode_args(const float* q, const float* k_cache, const float* v_cache,
+                                const float* out, uint32_t num_heads, uint32_t kv_heads,
+                                uint32_t head_dim, uint32_t max_seq, uint32_t total_seq,
+                                float scale);
+
 cudaError_t launch_decode(const DecodeCall& call, const DecodePlan& plan, void* workspace,
                           cudaStream_t stream);
 

@@ -880,6 +880,12 @@ extern "C" attn_status_t attn_decode_noalloc(const float* q, const float* k_cach
                                              uint32_t head_dim, uint32_t max_seq,
                                              uint32_t total_seq, uint32_t window, float scale,
                                              void* stream) {
+    // The arguments are checked as attn_decode checks them before the
+    // scratch size is: a malformed call reports INVALID_ARG whatever its sizes.
+    const attn_status_t st = attn::check_decode_args(q, k_cache, v_cache, out, num_heads,
+                                                     kv_heads, head_dim, max_seq, total_seq,
+                                                     scale);
+    if (st != ATTN_OK) return st;
     const size_t need = attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window);
     if (need > kNoAllocScratchBytes) {
         char msg[160];

@@ -11,11 +11,15 @@ replicas that every step reads them cold from HBM (the replicas together
 exceed twice the 129 MB L2).  Steps run as CUDA-graph replays so that host
 launch overhead does not bound a 5-microsecond step.
 
-The same line carries the causal-prefill half of the metric (TFLOP/s of the
-tensor-core path on the 2048- and 16384-token prefill workloads), the
-roofline of the dominant kernel of each, an end-to-end number through the
-Python API with host buffers, the fp64 CPU oracle timed on the host cores,
-and the SM clocks sampled during the timed region.
+The same line ends with one compact object per named workload, cfg1 ... cfg5
+(the 64-token exact prefill, this decode call alone, the 2048-token
+tensor-core prefill, the windowed 32768-row decode after an append, the
+16384-token tensor-core prefill): value, unit, time per call, fraction of the
+roofline peak, max abs error against the fp64 oracle, and for the prefills
+the end-to-end figure.  Before them: the roofline of the dominant decode
+kernel, an end-to-end number through the Python API with host buffers, the
+fp64 CPU oracle timed on the host cores, the SM clocks sampled during the
+timed region, the full-cache decode and the 28-layer prefill stack.
 
 --impl reference times the oracle (the plain CPU definition) on the host
 cores instead, on the same workload, metric and unit.
@@ -346,13 +350,17 @@ class PrefillBench:
         import oracle
         c = self.c
         q, k, v = self.host
-        rows = workloads.sample_rows(c.m, c.seed, 16, 16, 32)
+        # every row of a short prompt; a seeded sample of rows of a long one
+        # (the full comparison of the long prompt is a GPU test of its own)
+        rows = None if c.m <= 4096 else workloads.sample_rows(c.m, c.seed, 16, 16, 32)
         ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), c.m, c.num_q_heads,
                                     c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride, rows=rows)
         self.call(0, torch.cuda.current_stream())
         torch.cuda.synchronize()
         got = self.o[0].view(c.m, c.q_stride)[:, : c.num_q_heads * c.head_dim]
-        got = got.cpu().numpy().reshape(c.m, c.num_q_heads, c.head_dim)[rows]
+        got = got.cpu().numpy().reshape(c.m, c.num_q_heads, c.head_dim)
+        if rows is not None:
+            got = got[rows]
         return float(np.abs(got - ref).max())
 
 
@@ -471,28 +479,49 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
     e2e_per_call = pipe_per_call
     h2d = (q.numel() + k.numel() + v.numel()) * 4
     d2h = q.numel() * 4
-    return {
-        "workload": shape.name,
-        "value": round(tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(per_call * 1e3, 4),
-        "calls": n, "flops_per_call": flops,
-        "dtype": "fp16 operands (round-to-nearest from fp32), fp32 accumulate and output",
-        "l2": (f"inputs {pb.R} rotating replicas" if pb.R > 1 else "inputs larger than 2x L2"),
-        "max_abs_err_sampled_rows": err,
-        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_key} ({peak_src}; fp16 dense peak = bf16 nominal)",
-                     "kernel": "attn_prefill_causal call (rounding pre-pass + prefill_tc_kernel)"},
-        "e2e": {"value": round(flops / e2e_per_call / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "method": f"a stream of {e_calls} independent prompts: per call, H2D of Q, K, V "
-                          "from page-locked host memory, attn_prefill_causal, D2H of O; call "
-                          "n+1's H2D, call n and call n-1's D2H overlap on three streams "
-                          "(double-buffered device buffers); pipeline fill and drain included",
-                "ms_per_call": round(e2e_per_call * 1e3, 4),
-                "serial": {"value": round(flops / serial_per_call / 1e12, 2),
-                           "ms_per_call": round(serial_per_call * 1e3, 4)}},
-        "gpu_launches_per_call": pb.launches_per_call,
-    }
+    compact = {"value": round(tflops, 2), "unit": "TFLOP/s", "us": round(per_call * 1e6, 2),
+               "frac": round(tflops / peak, 4), "err": float(f"{err:.3g}"),
+               "e2e": round(flops / e2e_per_call / 1e12, 2),
+               "launches": pb.launches_per_call}
+    detail = {"workload": shape.name, "calls": n, "flops_per_call": flops,
+              "peak": peak, "peak_source": f"{peak_key} ({peak_src})", "traffic": traffic,
+              "l2": (f"inputs {pb.R} rotating replicas" if pb.R > 1 else "inputs larger than 2x L2"),
+              "e2e_pipelined_ms": round(e2e_per_call * 1e3, 4),
+              "e2e_serial_ms": round(serial_per_call * 1e3, 4),
+              "e2e_calls": e_calls, "h2d_bytes_per_call": h2d, "d2h_bytes_per_call": d2h}
+    return compact, detail
+
+
+# ---------------------------------------------------------------- copy floor (context)
+
+def copy_floor_us(replicas, traffic_bytes, stream, reps=50):
+    """Device time of a torch copy that moves the same number of DRAM bytes
+    as one decode call reads (half read, half written), rotating over the
+    cache replicas so that every copy reads cold, as CUDA-graph replays.
+    The measured HBM peak is this same copy at 1 Gi elements; at a decode's
+    size the copy shows what launch latency and ramp-up leave of it."""
+    n = traffic_bytes // 8  # floats read (= floats written)
+    srcs = [r.reshape(-1)[:n] for r in replicas]
+    dst = torch.empty(n, dtype=torch.float32, device=srcs[0].device)
+
+    def run():
+        for s in srcs:
+            dst.copy_(s)
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    g = make_graph(run, stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * len(srcs))
 
 
 # ---------------------------------------------------------------- companion workloads
@@ -512,18 +541,17 @@ def bench_decode_companion(attn, shape, device, stream, steps, peaks, peak_src):
     live = shape.kv_bytes_algorithmic()
     hbm = float(peaks["hbm_gbs"])
     gbs = live / per / 1e9
-    return {"workload": shape.name, "value": round(gbs, 2), "unit": "GB/s",
-            "ms_per_step": round(per * 1e3, 5), "steps": n,
-            "bytes_per_step": live, "bytes_all_rows": shape.kv_bytes_all_rows(),
-            "gbs_all_rows_formula": round(shape.kv_bytes_all_rows() / per / 1e9, 2),
-            "l2": f"{db.R} rotating cache replicas (live bytes {db.R * live // 2**20} MiB)",
-            "parity_max_abs_err": err,
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4),
-                         "traffic": traffic_for(f"attn_decode:{shape.name}", ["decode.cu"]),
-                         "peak_source": f"hbm_gbs ({peak_src})",
-                         "kernel": "attn_decode_append: decode_kernel + decode_combine_kernel"},
-            "gpu_launches_per_step": db.launches_per_step}
+    compact = {"value": round(gbs, 2), "unit": "GB/s", "us": round(per * 1e6, 3),
+               "frac": round(gbs / hbm, 4), "err": float(f"{err:.3g}")}
+    if shape.window:
+        compact["copy_floor_us"] = round(copy_floor_us(db.kc, live, stream), 3)
+    detail = {"workload": shape.name, "steps": n, "bytes_per_step": live,
+              "bytes_all_rows": shape.kv_bytes_all_rows(),
+              "gbs_all_rows_formula": round(shape.kv_bytes_all_rows() / per / 1e9, 2),
+              "l2": f"{db.R} rotating cache replicas (live bytes {db.R * live // 2**20} MiB)",
+              "traffic": traffic_for(f"attn_decode:{shape.name}", ["decode.cu"]),
+              "peak_source": f"hbm_gbs ({peak_src})", "launches_per_step": db.launches_per_step}
+    return compact, detail
 
 
 def fp32_peak_tflops(sm_count, clock_mhz):
@@ -572,13 +600,9 @@ def bench_prefill_fp32_small(attn, shape, device, stream, calls, peaks):
     tf = shape.flops() / per / 1e12
     props = torch.cuda.get_device_properties(device)
     peak = fp32_peak_tflops(props.multi_processor_count, float(peaks.get("sm_max_mhz", 2070.0)))
-    return {"workload": shape.name, "value": round(tf, 4), "unit": "TFLOP/s",
-            "us_per_call": round(per * 1e6, 3), "calls": reps * 32, "flops_per_call": shape.flops(),
-            "dtype": "fp32 CUDA cores", "max_abs_err": err, "l2": "inputs L2-resident (98 KB)",
-            "roofline": {"bound": "alu", "achieved": round(tf, 4), "peak": round(peak, 1),
-                         "unit": "TFLOP/s", "frac": round(tf / peak, 5), "traffic": None,
-                         "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock",
-                         "kernel": "prefill_fp32_kernel (latency-bound at this size)"}}
+    rel = err / float(np.abs(ref).max())
+    return {"value": round(tf, 4), "unit": "TFLOP/s", "us": round(per * 1e6, 3),
+            "frac": round(tf / peak, 5), "err": float(f"{err:.3g}"), "rel": float(f"{rel:.3g}")}
 
 
 # ---------------------------------------------------------------- layer stack (launch cost)
@@ -620,13 +644,8 @@ def bench_layer_stack(attn, shape, device, stream, layers=28, reps=5):
     eager_ms, eager_host_ms = timed(one_pass)
     g = make_graph(one_pass, stream)
     graph_ms, graph_host_ms = timed(g.replay)
-    return {"workload": f"{layers} layers x {shape.name}", "layers": layers,
-            # per layer: rounding pre-pass, main kernel, and the combine of the
-            # split key walk (this workload splits it)
-            "launches_per_pass": 3 * layers,
-            "eager_ms_per_pass": round(eager_ms, 4), "graph_ms_per_pass": round(graph_ms, 4),
-            "eager_host_ms_per_pass": round(eager_host_ms, 4),
-            "graph_host_ms_per_pass": round(graph_host_ms, 4)}
+    return {"eager_ms": round(eager_ms, 4), "graph_ms": round(graph_ms, 4),
+            "eager_host_ms": round(eager_host_ms, 4)}
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -708,18 +727,19 @@ def our_arm(args):
     if args.only in ("prefill_2k", "prefill_16k"):
         # Profiling aid: one prefill workload alone (no headline line).
         ps = workloads.PREFILL_2K if args.only == "prefill_2k" else workloads.PREFILL_16K
-        res = bench_prefill(attn, ps, device, stream, 200 if ps.m <= 4096 else 20, peaks, peak_src)
+        res, det = bench_prefill(attn, ps, device, stream, 200 if ps.m <= 4096 else 20, peaks,
+                                 peak_src)
         if rank == 0:
-            print(json.dumps({"only": args.only, "prefill": [res]}), flush=True)
+            print(json.dumps({"only": args.only, "result": res, "detail": det}), flush=True)
         return 0
     if args.only in ("decode_32k_window", "decode_32k_stream"):
         # Profiling aid: one 32768-row decode workload alone (no headline line).
         cs = (workloads.DECODE_32K_WINDOW if args.only == "decode_32k_window"
               else workloads.DECODE_32K_STREAM)
-        res = bench_decode_companion(attn, cs, device, stream,
-                                     2000 if cs.window else 200, peaks, peak_src)
+        res, det = bench_decode_companion(attn, cs, device, stream,
+                                          2000 if cs.window else 200, peaks, peak_src)
         if rank == 0:
-            print(json.dumps({"only": args.only, "other_workloads": [res]}), flush=True)
+            print(json.dumps({"only": args.only, "result": res, "detail": det}), flush=True)
         return 0
     shape = workloads.DECODE_4K
     db = DecodeBench(attn, shape, device)
@@ -763,32 +783,9 @@ def our_arm(args):
     hbm = float(peaks["hbm_gbs"])
     traffic = traffic_for(f"attn_decode:{shape.name}", ["decode.cu"])
 
-    # Context for the small workload: a plain read of the same bytes (torch
-    # reductions over the same L2-cold replicas, CUDA-graph replays).  Not our
-    # kernel: it shows how close any reader of 8 MB per step can get to peak.
-    def read_only():
-        for r in range(db.R):
-            torch.sum(db.kc[r], dtype=torch.float32)
-            torch.sum(db.vc[r], dtype=torch.float32)
-    with torch.cuda.stream(stream):
-        read_only()
-    torch.cuda.synchronize()
-    gro = make_graph(read_only, stream)
-    for _ in range(3):
-        gro.replay()
-    torch.cuda.synchronize()
-    r0e, r1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        r0e.record(stream)
-        for _ in range(50):
-            gro.replay()
-        r1e.record(stream)
-    r1e.synchronize()
-    read_s = r0e.elapsed_time(r1e) / 1e3 / (50 * db.R)
-    read_floor = {"what": "torch.sum over the same K and V replicas (2 reductions per step), "
-                          "CUDA-graph replays, L2-cold",
-                  "us_per_step": round(read_s * 1e6, 3),
-                  "gbs": round(bytes_step / read_s / 1e9, 1)}
+    # Context for the small workload: a torch copy moving the same number of
+    # DRAM bytes (the measurement that defines the HBM peak, at this size).
+    floor_us = copy_floor_us(db.kc, bytes_step, stream)
 
     # End to end through the Python API.  Every step takes its q, k_new and
     # v_new from page-locked host memory and leaves its output in page-locked
@@ -871,22 +868,28 @@ def our_arm(args):
                       "us_per_step": round(sec / n * 1e6, 3), "steps": n}
                   for k, (sec, n) in e_var.items()}
 
-    prefill = []
+    # The other workloads, each as one compact object (cfg1 ... cfg5 in the
+    # order of the five named workloads); details go to stderr with --detail.
+    cfgs, details = {}, {}
     if not args.no_prefill and args.only == "all":
-        for ps in (workloads.PREFILL_2K, workloads.PREFILL_16K):
-            calls = 200 if ps.m <= 4096 else 20
-            prefill.append(bench_prefill(attn, ps, device, stream, calls, peaks, peak_src))
-
-    layer_stack = None
-    companions = []
+        cfgs["cfg1"] = bench_prefill_fp32_small(attn, workloads.PREFILL_SMALL, device, stream,
+                                                3200, peaks)
+    cfgs["cfg2"] = {"value": round(achieved, 2), "unit": "GB/s", "us": round(per_decode * 1e6, 3),
+                    "frac": round(achieved / hbm, 4), "err": float(f"{err:.3g}"),
+                    "copy_floor_us": round(floor_us, 3)}
     if not args.no_prefill and args.only == "all":
-        layer_stack = bench_layer_stack(attn, workloads.PREFILL_2K, device, stream)
-        companions.append(bench_decode_companion(attn, workloads.DECODE_32K_WINDOW, device,
-                                                 stream, 2000, peaks, peak_src))
-        companions.append(bench_decode_companion(attn, workloads.DECODE_32K_STREAM, device,
-                                                 stream, 200, peaks, peak_src))
-        companions.append(bench_prefill_fp32_small(attn, workloads.PREFILL_SMALL, device,
-                                                   stream, 3200, peaks))
+        cfgs["cfg3"], details["cfg3"] = bench_prefill(attn, workloads.PREFILL_2K, device, stream,
+                                                      200, peaks, peak_src)
+        cfgs["cfg4"], details["cfg4"] = bench_decode_companion(
+            attn, workloads.DECODE_32K_WINDOW, device, stream, 2000, peaks, peak_src)
+        cfgs["cfg5"], details["cfg5"] = bench_prefill(attn, workloads.PREFILL_16K, device, stream,
+                                                      20, peaks, peak_src)
+        stream32k, details["stream32k"] = bench_decode_companion(
+            attn, workloads.DECODE_32K_STREAM, device, stream, 200, peaks, peak_src)
+        cfgs_extra = {"stream32k": {"value": stream32k["value"], "frac": stream32k["frac"]},
+                      "layers28": bench_layer_stack(attn, workloads.PREFILL_2K, device, stream)}
+    else:
+        cfgs_extra = {}
 
     status = attn.attn_get_device_status()
     if status != attn.ATTN_OK:
@@ -897,8 +900,7 @@ def our_arm(args):
         steps_c, secs_c, cores = cpu_baseline_decode(shape)
         cpu = {"value": round(bytes_step * steps_c / secs_c / 1e9, 3), "unit": "GB/s",
                "cores": cores, "kind": "oracle",
-               "sample": f"{steps_c} full decode steps (kv_append + decode, all heads) "
-                         f"in {secs_c:.1f} s"}
+               "sample": f"{steps_c} decode steps (append + all heads) in {secs_c:.1f} s"}
 
     if rank == 0:
         line = {
@@ -908,39 +910,26 @@ def our_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": shape.name, "num_heads": shape.num_heads,
                        "kv_heads": shape.kv_heads, "head_dim": shape.head_dim,
-                       "max_seq": shape.max_seq, "total_seq": shape.total_seq,
-                       "window": shape.window,
-                       "step": "attn_decode_append: append at total_seq-1 + decode (decode "
-                               "kernel + PDL combine kernel), CUDA-graph replays",
-                       "l2": f"inputs larger than L2: {db.R} rotating cache replicas "
-                             f"({db.R * 2 * shape.kv_heads * shape.max_seq * shape.head_dim * 4 // 2**20} MiB)",
-                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-
-                       "bytes_per_step": bytes_step},
+                       "total_seq": shape.total_seq, "window": shape.window,
+                       "step": "attn_decode_append, CUDA-graph replays",
+                       "l2": f"inputs larger than L2: {db.R} cache replicas",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
-                         "peak_source": f"hbm_gbs ({peak_src})",
-                         "kernel": "attn_decode call: decode_kernel + decode_combine_kernel (PDL)",
-                         "ms_per_launch": round(per_decode * 1e3, 5)},
+                         "peak_source": f"hbm_gbs ({peak_src})", "kernel": "attn_decode call"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e_bytes / e_max / 1e9, 3), "unit": "GB/s",
                     "h2d_bytes_per_step": (q.numel() + kn.numel() + vn.numel()) * 4,
-                    "d2h_bytes_per_step": shape.num_heads * shape.head_dim * 4,
-                    "method": "one attn_decode_append Python call per step with q, k_new, "
-                              "v_new and out in page-locked host memory: the call copies the "
-                              "inputs into its workspace with one small kernel and writes out "
-                              "over the CPU-GPU link, no memcpy; the K/V caches stay resident "
-                              "in HBM (decode state)",
-                    "variants": e_variants},
+                    "d2h_bytes_per_step": shape.num_heads * shape.head_dim * 4},
             "gpu_launches": args.steps * db.launches_per_step,
             "clocks": clocks,
-            "parity_max_abs_err": err,
-            "plain_read_same_bytes": read_floor,
-            "prefill": prefill,
-            "layer_stack": layer_stack,
-            "other_workloads": companions,
         }
+        line.update(cfgs_extra)
+        line.update(cfgs)
         print(json.dumps(line), flush=True)
+        if args.detail:
+            details["e2e_variants"] = e_variants
+            print(json.dumps(details), file=sys.stderr, flush=True)
     barrier(ws)
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -955,6 +944,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--detail", action="store_true",
+                    help="also print the per-workload details as JSON on stderr")
     ap.add_argument("--only", choices=["all", "decode", "prefill_2k", "prefill_16k",
                                        "decode_32k_window", "decode_32k_stream"],
                     default="all", help="profiling aid: run one workload only")

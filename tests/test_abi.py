@@ -119,6 +119,28 @@ def test_decode_rejects_bad_arguments(attn, kw, expect):
 
 
 @pytest.mark.parametrize("kw,expect", [
+    (dict(out=0), 1),                      # null output, at sizes beyond the scratch
+    (dict(q=FAKE + 4), 1),                 # misaligned, at sizes beyond the scratch
+    (dict(kv_heads=5000), 1),              # does not divide num_heads
+    (dict(total_seq=0), 1),
+    (dict(head_dim=96), 2),                # valid, outside the compiled head_dims
+    (dict(), 2),                           # well-formed, but its partials exceed the scratch
+])
+def test_decode_noalloc_checks_arguments_before_its_scratch_size(attn, kw, expect):
+    """The no-workspace decode validates its arguments exactly as attn_decode
+    does before it looks at its fixed scratch size, so a malformed call is
+    reported as INVALID_ARG whatever its sizes (no device work is launched
+    for a rejected call)."""
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, num_heads=8192, kv_heads=8192, head_dim=128,
+             max_seq=1, total_seq=1, window=0, scale=0.0)
+    a.update(kw)
+    st = attn.lib.attn_decode_noalloc(a["q"], a["k"], a["v"], a["out"], a["num_heads"],
+                                      a["kv_heads"], a["head_dim"], a["max_seq"], a["total_seq"],
+                                      a["window"], a["scale"], None)
+    assert st == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
     (dict(position=4096), 1),              # position >= max_seq
     (dict(v_src=None), 1),                 # v_src and v_cache must both be given or both null
     (dict(k_src=0), 1),
