@@ -18,6 +18,7 @@ import re
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
     "ATTN_ERR_TIMEOUT", "ATTN_ERR_RANGE", "ATTN_PREC_FP32", "ATTN_PREC_FP16", "ATTN_PREC_BF16",
+    "ATTN_PREC_TF32",
     "AttnError", "lib", "library_path", "attn_prefill_causal", "attn_prefill_workspace_size",
     "attn_decode", "attn_decode_workspace_size", "attn_decode_append", "attn_decode_noalloc",
     "kv_append", "attn_status_string",
@@ -27,7 +28,7 @@ __all__ = [
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA = 0, 1, 2, 3
 ATTN_ERR_TIMEOUT, ATTN_ERR_RANGE = 4, 5
-ATTN_PREC_FP32, ATTN_PREC_FP16, ATTN_PREC_BF16 = 0, 1, 2
+ATTN_PREC_FP32, ATTN_PREC_FP16, ATTN_PREC_BF16, ATTN_PREC_TF32 = 0, 1, 2, 3
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_PKG, "libattn.so")

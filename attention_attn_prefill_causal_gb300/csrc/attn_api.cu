@@ -128,15 +128,17 @@ const char* attn_status_string(attn_status_t status) {
 const char* attn_last_error_string(void) { return t_last_error; }
 
 size_t attn_prefill_workspace_size(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
-                                   uint32_t head_dim, int precision) {
+                                   uint32_t head_dim, attn_precision_t precision) {
     if (precision == ATTN_PREC_FP32) return 0;
+    if (precision == ATTN_PREC_TF32)
+        return prefill_tf32_workspace_bytes(m, num_q_heads, num_kv_heads, head_dim);
     return prefill_tc_workspace_bytes(m, num_q_heads, num_kv_heads, head_dim);
 }
 
 attn_status_t attn_prefill_causal(const float* q, const float* k, const float* v, float* o,
                                   uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
-                                  float scale, int precision, void* workspace,
+                                  float scale, attn_precision_t precision, void* workspace,
                                   size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
     if (num_q_heads == 0 || num_kv_heads == 0 || num_q_heads % num_kv_heads != 0)
@@ -150,7 +152,7 @@ attn_status_t attn_prefill_causal(const float* q, const float* k, const float* v
         return ATTN_ERR_INVALID_ARG;
     if (!(scale >= 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     if (precision != ATTN_PREC_FP32 && precision != ATTN_PREC_FP16 &&
-        precision != ATTN_PREC_BF16)
+        precision != ATTN_PREC_BF16 && precision != ATTN_PREC_TF32)
         return ATTN_ERR_INVALID_ARG;
     if (m == 0) return ATTN_OK;
     const float sc = resolve_scale(scale, head_dim);
@@ -163,15 +165,19 @@ attn_status_t attn_prefill_causal(const float* q, const float* k, const float* v
     if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     // TMA tiles address rows with 32-bit coordinates.
     if (m > 0x7fffffffu) return ATTN_ERR_UNSUPPORTED;
-    const size_t need = prefill_tc_workspace_bytes(m, num_q_heads, num_kv_heads, head_dim);
+    const size_t need = attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim,
+                                                    precision);
     if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_INVALID_ARG;
     unsigned int* status = device_status_ptr();
     if (!status) return record_cuda_error(cudaGetLastError());
-    const cudaError_t e = launch_prefill_tc(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim,
-                                            q_stride, kv_stride, sc,
-                                            precision == ATTN_PREC_BF16, workspace, status,
-                                            wait_limit_ns(), st);
+    const cudaError_t e =
+        precision == ATTN_PREC_TF32
+            ? launch_prefill_tf32(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_stride,
+                                  kv_stride, sc, workspace, status, wait_limit_ns(), st)
+            : launch_prefill_tc(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_stride,
+                                kv_stride, sc, precision == ATTN_PREC_BF16, workspace, status,
+                                wait_limit_ns(), st);
     if (e == cudaErrorNotSupported) {
         std::snprintf(t_last_error, sizeof(t_last_error),
                       "cuTensorMapEncodeTiled unavailable or rejected the operand layout");

@@ -111,6 +111,16 @@ cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, fl
                               float scale, bool bf16, void* workspace, unsigned int* status,
                               uint64_t wait_limit_ns, cudaStream_t stream);
 
+size_t prefill_tf32_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                    uint32_t head_dim);
+
+// TF32 tensor-core prefill; cudaErrorNotSupported as launch_prefill_tc.
+cudaError_t launch_prefill_tf32(const float* q, const float* k, const float* v, float* o,
+                                uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
+                                float scale, void* workspace, unsigned int* status,
+                                uint64_t wait_limit_ns, cudaStream_t stream);
+
 cudaError_t launch_wait_timeout_selftest(unsigned int* status, uint64_t limit_ns);
 
 }  // namespace attn

@@ -63,6 +63,7 @@
 #include <mutex>
 
 #include "attn_internal.h"
+#include "prefill_tc_common.cuh"
 #include "sm103_ptx.cuh"
 
 namespace attn {
@@ -70,18 +71,13 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBM = 128;            // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;            // keys per KV tile
-constexpr int kNQ = 2;              // query tiles per CTA
 constexpr int kStages = 2;          // K/V ring depth
 constexpr int kThreads = 320;
 constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint64_t kDrainWaitNs = 100000000ull;  // 100 ms: copies/MMAs in flight finish in us
 
 template <int D>
 struct TcLayout {
@@ -122,12 +118,6 @@ struct __align__(8) TcBarriers {
     uint32_t abort;
 };
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 __device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16) {
     if (bf16) {
         __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -140,25 +130,6 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16) {
 __device__ __forceinline__ void record_timeout(unsigned int* status, TcBarriers* bars) {
     atomicOr(status, kStatusTimeout);
     atomicExch(&bars->abort, 1u);
-}
-
-// Split-KV scheduling for small grids: a query-tile pair's keys are walked in
-// chunks of kv_chunk tiles by separate CTAs; split pairs leave per-chunk
-// partials that prefill_combine_kernel merges.  kv_chunk = ~0u: no split.
-constexpr uint32_t kNoSplit = 0xffffffffu;
-
-struct SplitArgs {
-    uint32_t kv_chunk;
-    uint32_t n_chunks_max;
-    uint32_t first_split_row;  // rows >= this belong to split pairs
-    uint32_t m_pad;            // rows rounded up to whole query tiles
-    float* part_o;             // [n_chunks_max, heads, m_pad, D] unnormalised
-    float* part_ml;            // [n_chunks_max, heads, m_pad, 2] (max in log2 units, sum)
-};
-
-// Number of KV tiles query tile `qt` attends to (0 when the tile is empty).
-__device__ __forceinline__ uint32_t kv_tiles_for(uint32_t qt, uint32_t m) {
-    return (qt * kBM < m) ? qt + 1 : 0;  // kBN == kBM: the diagonal tile index is qt
 }
 
 template <int D, bool BF16>
@@ -187,7 +158,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else {
         uint32_t idx = blockIdx.x / num_q_heads;
         for (int p = (int)n_pairs - 1; p >= 0; --p) {
-            const uint32_t nk = max(kv_tiles_for(p * kNQ, m), kv_tiles_for(p * kNQ + 1, m));
+            const uint32_t nk = max(kv_tiles_for(p * kNQ, m, 1), kv_tiles_for(p * kNQ + 1, m, 1));
             const uint32_t nc = (nk + split.kv_chunk - 1) / split.kv_chunk;
             if (idx < nc) {
                 pair = (uint32_t)p;
@@ -201,7 +172,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t qt0 = pair * kNQ;                                // first query tile index
     uint32_t n_kv[kNQ];
 #pragma unroll
-    for (int t = 0; t < kNQ; ++t) n_kv[t] = kv_tiles_for(qt0 + t, m);
+    for (int t = 0; t < kNQ; ++t) n_kv[t] = kv_tiles_for(qt0 + t, m, 1);
     uint32_t n_kv_pair = 0;
 #pragma unroll
     for (int t = 0; t < kNQ; ++t) n_kv_pair = max(n_kv_pair, n_kv[t]);
@@ -604,78 +575,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
-// Merge of the KV-chunk partials of split query-tile pairs.  A thread owns 8
-// consecutive elements of one (row, head); the 16 (D = 128) threads of a row
-// read and write whole 512-byte rows.  Up to kCombineBatch chunks are merged
-// per round trip: every load of a batch is issued before any is used.
-// Launched as a programmatic dependent of the prefill kernel.
-constexpr uint32_t kCombineBatch = 4;
-
-template <int D>
-__global__ void __launch_bounds__(256)
-prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
-                       uint32_t num_q_heads, uint32_t q_stride) {
-    constexpr uint32_t kPerRow = D / 8;  // threads per (row, head)
-    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
-    const uint32_t item = tid / kPerRow, e0 = (tid % kPerRow) * 8;
-    const uint32_t row = split.first_split_row + item / num_q_heads;
-    const uint32_t h = item % num_q_heads;
-    if (row >= m) return;
-    const uint32_t n_kv_tile = row / kBM + 1;  // KV tiles of this row's query tile
-    const uint32_t nct = (n_kv_tile + split.kv_chunk - 1) / split.kv_chunk;
-    // partial (c, h, row) sits at index (c * num_q_heads + h) * m_pad + row
-    const size_t base = (size_t)h * split.m_pad + row;
-    const size_t cstride = (size_t)num_q_heads * split.m_pad;
-    float M = -CUDART_INF_F, L = 0.f, O[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) O[i] = 0.f;
-    for (uint32_t c0 = 0; c0 < nct; c0 += kCombineBatch) {
-        float2 ml[kCombineBatch];
-        float4 lo[kCombineBatch], hi[kCombineBatch];
-#pragma unroll
-        for (uint32_t b = 0; b < kCombineBatch; ++b) {
-            const uint32_t c = c0 + b;
-            if (c < nct) {
-                const size_t pidx = base + c * cstride;
-                ml[b] = __ldcg(reinterpret_cast<const float2*>(split.part_ml) + pidx);
-                const float4* po = reinterpret_cast<const float4*>(split.part_o + pidx * D + e0);
-                lo[b] = __ldcg(po);
-                hi[b] = __ldcg(po + 1);
-            } else {
-                ml[b] = make_float2(-CUDART_INF_F, 0.f);
-                lo[b] = hi[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        float Mb = M;
-#pragma unroll
-        for (uint32_t b = 0; b < kCombineBatch; ++b) Mb = fmaxf(Mb, ml[b].x);
-        const float fo = ex2(M - Mb);  // M = -inf on the first batch: 0
-        L *= fo;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) O[i] *= fo;
-#pragma unroll
-        for (uint32_t b = 0; b < kCombineBatch; ++b) {
-            const float f = ex2(ml[b].x - Mb);  // -inf (absent chunk): 0
-            L = fmaf(ml[b].y, f, L);
-            O[0] = fmaf(lo[b].x, f, O[0]);
-            O[1] = fmaf(lo[b].y, f, O[1]);
-            O[2] = fmaf(lo[b].z, f, O[2]);
-            O[3] = fmaf(lo[b].w, f, O[3]);
-            O[4] = fmaf(hi[b].x, f, O[4]);
-            O[5] = fmaf(hi[b].y, f, O[5]);
-            O[6] = fmaf(hi[b].z, f, O[6]);
-            O[7] = fmaf(hi[b].w, f, O[7]);
-        }
-        M = Mb;
-    }
-    const float inv = 1.0f / L;
-    float4* dst = reinterpret_cast<float4*>(o + (size_t)row * q_stride + (size_t)h * D + e0);
-    dst[0] = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-    dst[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
-}
-
 // fp32 -> fp16/bf16 rounding pre-pass for the keys and values: k [m,
 // kv_stride] -> kh [m, hkv*d], likewise v (the queries are rounded inside the
 // prefill kernel, each tile once).  grid.y selects the tensor (0 = k, 1 = v).
@@ -733,20 +632,8 @@ __global__ void wait_timeout_selftest_kernel(unsigned int* status, uint64_t wait
     if (!mbar_wait(smem_u32(&bar), 0, wait_ns, status, kStatusTimeout)) atomicOr(status, kStatusTimeout);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
+// fp16/bf16 operand map: tight rows of `cols` elements, boxes of 64
+// elements (128 bytes) x box_rows, 128-byte swizzle.
 bool encode_operand_map(CUtensorMap* map, const void* base, uint32_t cols, uint32_t rows,
                         uint32_t box_rows, bool bf16) {
     auto enc = tensor_map_encoder();
@@ -762,71 +649,9 @@ bool encode_operand_map(CUtensorMap* map, const void* base, uint32_t cols, uint3
     return r == CUDA_SUCCESS;
 }
 
-// fp32 output map for the epilogue's TMA stores: rows of `cols` floats with a
-// pitch of `row_stride` floats, boxes of 32 floats x box_rows, 128-byte swizzle.
-bool encode_output_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
-                       uint64_t row_stride, uint32_t box_rows) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t gdim[2] = {cols, rows};
-    cuuint64_t gstride[1] = {row_stride * 4};
-    cuuint32_t box[2] = {32, box_rows};
-    cuuint32_t estride[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gdim,
-                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-struct PrefillPlan {
-    uint32_t n_items;          // work items per head (pairs, or pair chunks)
-    SplitArgs split;           // kv_chunk == kNoSplit: no split
-    size_t operand_bytes;      // fp16 K, V
-    size_t part_o_bytes, part_ml_bytes;
-};
-
-// Split the KV walk only when the pairs alone leave SMs idle: then take the
-// smallest chunk (most parallelism, shortest item) whose items still fit in
-// one wave.  nk(p) = KV tiles of pair p's second tile.
-PrefillPlan make_plan(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
-                      int sm_count) {
-    PrefillPlan p{};
-    const uint32_t n_qt = (m + kBM - 1) / kBM;
-    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
-    auto nk = [&](uint32_t pr) { return std::min(kNQ * pr + kNQ, n_qt); };
-    p.n_items = n_pairs;
-    p.split.kv_chunk = kNoSplit;
-    p.split.n_chunks_max = 1;
-    p.split.first_split_row = m;
-    p.split.m_pad = n_qt * kBM;
-    const uint32_t sms = (uint32_t)std::max(sm_count, 1);
-    if (n_pairs > 0 && (uint64_t)n_pairs * num_q_heads < sms) {
-        const uint32_t nk_last = nk(n_pairs - 1);
-        for (uint32_t c = 2; c < nk_last; ++c) {
-            uint32_t items = 0;
-            for (uint32_t pr = 0; pr < n_pairs; ++pr) items += (nk(pr) + c - 1) / c;
-            if ((uint64_t)items * num_q_heads <= sms) {
-                p.n_items = items;
-                p.split.kv_chunk = c;
-                p.split.n_chunks_max = (nk_last + c - 1) / c;
-                uint32_t first = 0;
-                while (first < n_pairs && nk(first) <= c) ++first;
-                p.split.first_split_row = std::min(m, first * kNQ * kBM);
-                break;
-            }
-        }
-    }
-    const size_t kb = (size_t)m * num_kv_heads * head_dim * 2;
-    p.operand_bytes = 2 * align256(kb);
-    if (p.split.kv_chunk != kNoSplit) {
-        const size_t rows = (size_t)p.split.n_chunks_max * num_q_heads * p.split.m_pad;
-        p.part_o_bytes = align256(rows * head_dim * 4);
-        p.part_ml_bytes = align256(rows * 2 * 4);
-    }
-    return p;
+// Workspace bytes of the rounded fp16/bf16 K and V (each 256-byte aligned).
+size_t operand_bytes_16(uint32_t m, uint32_t num_kv_heads, uint32_t head_dim) {
+    return 2 * align256((size_t)m * num_kv_heads * head_dim * 2);
 }
 
 template <int D, bool BF16>
@@ -835,14 +660,15 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
                       uint32_t kv_stride, float scale, void* workspace, unsigned int* status,
                       uint64_t wait_ns, cudaStream_t stream) {
     using L = TcLayout<D>;
-    const PrefillPlan plan = make_plan(m, num_q_heads, num_kv_heads, D, device_sm_count());
+    const PrefillPlan plan = make_plan(m, num_q_heads, D, device_sm_count(), 1);
+    const size_t operand_bytes = operand_bytes_16(m, num_kv_heads, D);
     const uint32_t q_cols = num_q_heads * D, kv_cols = num_kv_heads * D;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     uint16_t* kh = reinterpret_cast<uint16_t*>(ws);
     uint16_t* vh = reinterpret_cast<uint16_t*>(ws + align256((size_t)m * kv_cols * 2));
     SplitArgs split = plan.split;
-    split.part_o = reinterpret_cast<float*>(ws + plan.operand_bytes);
-    split.part_ml = reinterpret_cast<float*>(ws + plan.operand_bytes + plan.part_o_bytes);
+    split.part_o = reinterpret_cast<float*>(ws + operand_bytes);
+    split.part_ml = reinterpret_cast<float*>(ws + operand_bytes + plan.part_o_bytes);
 
     {
         const size_t work = (size_t)m * kv_cols / 8;
@@ -908,8 +734,8 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
 
 size_t prefill_tc_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim) {
-    const PrefillPlan p = make_plan(m, num_q_heads, num_kv_heads, head_dim, device_sm_count());
-    return p.operand_bytes + p.part_o_bytes + p.part_ml_bytes;
+    const PrefillPlan p = make_plan(m, num_q_heads, head_dim, device_sm_count(), 1);
+    return operand_bytes_16(m, num_kv_heads, head_dim) + p.part_o_bytes + p.part_ml_bytes;
 }
 
 cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, float* o,

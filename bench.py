@@ -319,9 +319,16 @@ def remainder_graphs(bench, stream, append=True):
 
 # ---------------------------------------------------------------- prefill (companion)
 
+# Dense tensor peaks relative to the 16-bit one (nominal GB300 figures:
+# 2.25 PFLOP/s fp16/bf16, 1.1 PFLOP/s tf32); the measured bf16 peak is
+# scaled by this ratio for the TF32 mode.
+TF32_PEAK_RATIO = 1.1 / 2.25
+
+
 class PrefillBench:
-    def __init__(self, attn, shape, device):
+    def __init__(self, attn, shape, device, precision=None):
         self.attn, self.c, self.dev = attn, shape, device
+        self.prec = attn.ATTN_PREC_FP16 if precision is None else precision
         q, k, v = workloads.shape_inputs(shape)
         self.host = (q, k, v)
         in_bytes = (q.numel() + k.numel() + v.numel() + q.numel()) * 4
@@ -331,20 +338,21 @@ class PrefillBench:
         self.v = [v.to(device) for _ in range(self.R)]
         self.o = [torch.empty_like(self.q[0]) for _ in range(self.R)]
         ws = attn.attn_prefill_workspace_size(shape.m, shape.num_q_heads, shape.num_kv_heads,
-                                              shape.head_dim, attn.ATTN_PREC_FP16)
+                                              shape.head_dim, self.prec)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
-        # The workspace holds the rounded K and V (two 256-byte aligned fp16
-        # matrices) and, when the call splits its key walk, the partials that
-        # a third kernel merges.
-        kv_bytes = shape.m * shape.num_kv_heads * shape.head_dim * 2
+        # The workspace holds the rounded K and V (two 256-byte aligned
+        # matrices of 2 bytes per element, 4 in the TF32 mode) and, when the
+        # call splits its key walk, the partials that a third kernel merges.
+        esize = 4 if self.prec == attn.ATTN_PREC_TF32 else 2
+        kv_bytes = shape.m * shape.num_kv_heads * shape.head_dim * esize
         operands = 2 * ((kv_bytes + 255) // 256 * 256)
-        self.launches_per_call = 3 if ws > operands else 2
+        self.launches_per_call = 3 if ws > operands + 512 else 2
 
     def call(self, i, stream):
         c, a, r = self.c, self.attn, i % self.R
         a.attn_prefill_causal(self.q[r], self.k[r], self.v[r], self.o[r], c.m, c.num_q_heads,
                               c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride,
-                              precision=a.ATTN_PREC_FP16, workspace=self.ws, stream=stream)
+                              precision=self.prec, workspace=self.ws, stream=stream)
 
     def check(self):
         import oracle
@@ -362,6 +370,37 @@ class PrefillBench:
         if rows is not None:
             got = got[rows]
         return float(np.abs(got - ref).max())
+
+
+def bench_prefill_tf32(attn, shape, device, stream, calls, peaks, peak_src):
+    """The TF32 mode on a prefill workload: device time per call and its
+    fraction of the TF32 dense peak (no end-to-end leg)."""
+    pb = PrefillBench(attn, shape, device, attn.ATTN_PREC_TF32)
+    err = pb.check()
+
+    def chunk():
+        for i in range(pb.R):
+            pb.call(i, stream)
+    g = make_graph(chunk, stream)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, math.ceil(calls / pb.R))
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+    end.synchronize()
+    secs = start.elapsed_time(end) / 1e3
+    per_call = secs / (reps * pb.R)
+    tflops = shape.flops() / per_call / 1e12
+    peak_key = "bf16_tflops_sustained" if secs > 1.0 else "bf16_tflops"
+    peak = float(peaks[peak_key]) * TF32_PEAK_RATIO
+    return {"value": round(tflops, 2), "unit": "TFLOP/s", "us": round(per_call * 1e6, 2),
+            "frac": round(tflops / peak, 4), "peak": round(peak, 1), "err": float(f"{err:.3g}"),
+            "launches": pb.launches_per_call}
 
 
 def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
@@ -724,6 +763,14 @@ def our_arm(args):
 
     peaks, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=device)
+    if args.only in ("prefill_2k_tf32", "prefill_16k_tf32"):
+        # Profiling aid: the TF32 mode on one prefill workload alone.
+        ps = workloads.PREFILL_2K if args.only == "prefill_2k_tf32" else workloads.PREFILL_16K
+        res = bench_prefill_tf32(attn, ps, device, stream, 200 if ps.m <= 4096 else 10, peaks,
+                                 peak_src)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "result": res}), flush=True)
+        return 0
     if args.only in ("prefill_2k", "prefill_16k"):
         # Profiling aid: one prefill workload alone (no headline line).
         ps = workloads.PREFILL_2K if args.only == "prefill_2k" else workloads.PREFILL_16K
@@ -884,6 +931,10 @@ def our_arm(args):
             attn, workloads.DECODE_32K_WINDOW, device, stream, 2000, peaks, peak_src)
         cfgs["cfg5"], details["cfg5"] = bench_prefill(attn, workloads.PREFILL_16K, device, stream,
                                                       20, peaks, peak_src)
+        cfgs["cfg3_tf32"] = bench_prefill_tf32(attn, workloads.PREFILL_2K, device, stream, 200,
+                                               peaks, peak_src)
+        cfgs["cfg5_tf32"] = bench_prefill_tf32(attn, workloads.PREFILL_16K, device, stream, 10,
+                                               peaks, peak_src)
         stream32k, details["stream32k"] = bench_decode_companion(
             attn, workloads.DECODE_32K_STREAM, device, stream, 200, peaks, peak_src)
         cfgs_extra = {"stream32k": {"value": stream32k["value"], "frac": stream32k["frac"]},
@@ -947,6 +998,7 @@ def main(argv=None):
     ap.add_argument("--detail", action="store_true",
                     help="also print the per-workload details as JSON on stderr")
     ap.add_argument("--only", choices=["all", "decode", "prefill_2k", "prefill_16k",
+                                       "prefill_2k_tf32", "prefill_16k_tf32",
                                        "decode_32k_window", "decode_32k_stream"],
                     default="all", help="profiling aid: run one workload only")
     args = ap.parse_args(argv)

@@ -72,7 +72,14 @@ typedef enum {
     ATTN_PREC_FP16 = 1,
     /* As ATTN_PREC_FP16 with bf16 operands (8-bit mantissa): wider range,
      * larger rounding error. */
-    ATTN_PREC_BF16 = 2
+    ATTN_PREC_BF16 = 2,
+    /* Tensor-core mode with TF32 operands: tcgen05 kind::tf32 MMAs read fp32
+     * data and use its top 19 bits (fp32's exponent, a 10-bit mantissa).  Q
+     * is used as stored; K and V are rounded to nearest TF32 by a pre-pass
+     * into the workspace (V also transposed); P is written as fp32; fp32
+     * accumulation, softmax statistics and output.  No input range limit
+     * beyond fp32's own; half the 16-bit tensor rate.  head_dim in {64, 128}. */
+    ATTN_PREC_TF32 = 3
 } attn_precision_t;
 
 /*
@@ -99,20 +106,21 @@ typedef enum {
  * (the page's constructor assertion); q_stride >= num_q_heads*head_dim;
  * kv_stride >= num_kv_heads*head_dim; strides % 4 == 0.  m == 0 is a no-op.
  * ATTN_ERR_UNSUPPORTED: head_dim outside {32, 64, 128} (FP32) or
- * {64, 128} (FP16/BF16).
+ * {64, 128} (FP16/BF16/TF32).
  */
 attn_status_t attn_prefill_causal(const float* q, const float* k, const float* v, float* o,
                                   uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
-                                  float scale, int precision, void* workspace,
+                                  float scale, attn_precision_t precision, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
 /* Bytes of device workspace attn_prefill_causal needs for these sizes
- * (0 for ATTN_PREC_FP32): the fp16 K and V, plus per-chunk partials when
- * the call splits its key walk (small problems).  Depends only on the
- * arguments and on the current device's SM count. */
+ * (0 for ATTN_PREC_FP32): the rounded K and V (fp16/bf16, or TF32-rounded
+ * fp32 with V transposed), plus per-chunk partials when the call splits its
+ * key walk (small problems).  Depends only on the arguments and on the
+ * current device's SM count. */
 size_t attn_prefill_workspace_size(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
-                                   uint32_t head_dim, int precision);
+                                   uint32_t head_dim, attn_precision_t precision);
 
 /*
  * attn_decode -- single-query grouped-query attention against a K/V cache.

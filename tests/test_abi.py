@@ -61,6 +61,12 @@ def test_workspace_sizes_are_pure_functions(attn):
     ws = attn.attn_prefill_workspace_size(2048, 12, 2, 128, attn.ATTN_PREC_FP16)
     assert ws >= 2 * 2048 * (2 * 128) * 2       # fp16 K and V
     assert ws == attn.attn_prefill_workspace_size(2048, 12, 2, 128, attn.ATTN_PREC_FP16)
+    wt = attn.attn_prefill_workspace_size(2048, 12, 2, 128, attn.ATTN_PREC_TF32)
+    assert wt >= 2 * 2048 * (2 * 128) * 4       # TF32-rounded K and transposed V, fp32
+    assert wt == attn.attn_prefill_workspace_size(2048, 12, 2, 128, attn.ATTN_PREC_TF32)
+    # V^T rows are padded to a multiple of 4 keys (16-byte TMA row pitch)
+    assert attn.attn_prefill_workspace_size(1001, 4, 2, 64, attn.ATTN_PREC_TF32) >= \
+        1001 * 128 * 4 + 128 * 1004 * 4
     d = attn.attn_decode_workspace_size(12, 2, 128, 4096, 0)
     assert d > 12 * 128 * 4
     # a window shrinks the live range, so the workspace cannot grow
@@ -83,6 +89,9 @@ FAKE = 0x10000  # a 16-byte aligned non-null value; never dereferenced (rejected
     (dict(precision=7), 1),
     (dict(precision=1, head_dim=32), 2),              # tensor path: head_dim 64/128 only
     (dict(precision=1), 1),                           # tensor path without workspace
+    (dict(precision=3, head_dim=32), 2),              # TF32 path: head_dim 64/128 only
+    (dict(precision=3), 1),                           # TF32 path without workspace
+    (dict(precision=4), 1),
     (dict(precision=0, head_dim=96, q_stride=1152, kv_stride=192), 2),
     (dict(m=0), 0),                                   # empty prefill: no-op
 ])

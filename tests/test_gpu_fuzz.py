@@ -2,11 +2,11 @@
 
 Each case draws its shape from a fixed generator: GQA ratios from 1 to 16,
 head_dim 32/64/128, ragged token counts, padded row strides, explicit and
-default scales, the three prefill precisions (including token counts that
+default scales, the four prefill precisions (including token counts that
 make the tensor-core path split its key walk), and decode with windows,
 ragged lengths, the fused append and RoPE.  Tolerances are the ones the
-named tests use: fp32 max abs <= 1e-4 and normwise rel <= 1e-4; fp16
-operands max abs <= 3e-3; bf16 operands max abs <= 2.5e-2 (unit roundoff
+named tests use: fp32 max abs <= 1e-4 and normwise rel <= 1e-4; fp16 and
+tf32 operands max abs <= 3e-3; bf16 operands max abs <= 2.5e-2 (unit roundoff
 2^-9 on |V| up to about 4).  The rounding error of a score grows linearly
 with the scale (|ds| ~ scale |q| |k| u), so with an explicit scale above the
 default 1/sqrt(head_dim) the two operand-rounding bounds are multiplied by
@@ -22,8 +22,14 @@ from tests.parity_utils import (FP32_ABS, FP32_REL, TC_ABS, compare, guarded_emp
 
 pytestmark = pytest.mark.gpu
 
-FP32, FP16, BF16 = 0, 1, 2
+FP32, FP16, BF16, TF32 = 0, 1, 2, 3
 BF16_ABS = 2.5e-2
+
+
+def _tf32_variants(cases):
+    """Every tensor-core case again in the TF32 mode (same shape and inputs;
+    case ids offset by 500)."""
+    return [(c[0] + 500, TF32) + tuple(c[2:]) for c in cases if c[1] in (FP16, BF16)]
 
 
 def _prefill_cases(n=28, seed=20261203):
@@ -114,11 +120,13 @@ def attn():
     return a
 
 
-@pytest.mark.parametrize("case", _prefill_cases() + _wide_prefill_cases(), ids=lambda c: f"p{c[0]}")
+@pytest.mark.parametrize("case", _prefill_cases() + _wide_prefill_cases()
+                         + _tf32_variants(_prefill_cases() + _wide_prefill_cases()),
+                         ids=lambda c: f"p{c[0]}")
 def test_fuzz_prefill(attn, case):
     i, prec, m, hq, hkv, d, q_pad, kv_pad, mul, scale, big = case
     qs, kvs = hq * d + q_pad, hkv * d + kv_pad
-    q, k, v = workloads.prefill_inputs(m, qs, kvs, seed=1000 + i, mul=mul)
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, seed=1000 + i % 500, mul=mul)
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     buf, o = guarded_empty(m * qs)
     attn.attn_prefill_causal(dq, dk, dv, o, m, hq, hkv, d, qs, kvs, scale=scale, precision=prec)
@@ -136,7 +144,7 @@ def test_fuzz_prefill(attn, case):
         assert amax <= FP32_ABS and rel <= FP32_REL, (case, amax, rel)
     else:
         widen = max(1.0, scale * d ** 0.5)
-        assert amax <= (TC_ABS if prec == FP16 else BF16_ABS) * widen, (case, amax)
+        assert amax <= (BF16_ABS if prec == BF16 else TC_ABS) * widen, (case, amax)
 
 
 def _rope_tables(d, seed):

@@ -48,7 +48,7 @@ def _run(attn, inputs, prec):
     return got
 
 
-@pytest.mark.parametrize("prec_name", ["FP16", "FP32"])
+@pytest.mark.parametrize("prec_name", ["FP16", "TF32", "FP32"])
 def test_long_prefill_every_output_matches_oracle(inputs, reference, prec_name):
     import attention_attn_prefill_causal_gb300 as attn
     prec = getattr(attn, f"ATTN_PREC_{prec_name}")

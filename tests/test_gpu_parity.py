@@ -16,7 +16,7 @@ from tests.parity_utils import (FP32_ABS, FP32_REL, TC_ABS, compare, guarded_emp
 
 pytestmark = pytest.mark.gpu
 
-FP32, FP16 = 0, 1
+FP32, FP16, TF32 = 0, 1, 3
 
 
 @pytest.fixture(scope="module")
@@ -61,10 +61,11 @@ def test_workload_prefill_small_fp32(attn):
     print(f"{c.name}: max abs {amax:.3e} rel {rel:.3e}")
 
 
-def test_workload_prefill_2k_tensor_core(attn):
+@pytest.mark.parametrize("prec", [FP16, TF32])
+def test_workload_prefill_2k_tensor_core(attn, prec):
     c = workloads.PREFILL_2K
-    amax, rel = _check_prefill(attn, c.m, c.num_q_heads, c.num_kv_heads, c.head_dim, FP16, c.seed)
-    print(f"{c.name} fp16-operand tensor path: max abs {amax:.3e} rel {rel:.3e}")
+    amax, rel = _check_prefill(attn, c.m, c.num_q_heads, c.num_kv_heads, c.head_dim, prec, c.seed)
+    print(f"{c.name} tensor path (precision {prec}): max abs {amax:.3e} rel {rel:.3e}")
 
 
 def test_workload_prefill_2k_fp32(attn):
@@ -73,7 +74,7 @@ def test_workload_prefill_2k_fp32(attn):
     print(f"{c.name} fp32 path: max abs {amax:.3e} rel {rel:.3e}")
 
 
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 def test_workload_prefill_16k_sampled_rows(attn, prec):
     c = workloads.PREFILL_16K
     rows = workloads.sample_rows(c.m, c.seed)
@@ -138,14 +139,14 @@ def test_workload_append_then_windowed_decode_32k(attn):
 # ------------------------------------------------------------------ prefill edge cases
 
 @pytest.mark.parametrize("m", [1, 2, 31, 127, 128, 129, 255, 256, 257, 300, 511, 640])
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 def test_prefill_ragged_lengths(attn, m, prec):
     _check_prefill(attn, m, 4, 2, 128, prec, seed=100 + m)
 
 
 @pytest.mark.parametrize("hq,hkv", [(1, 1), (3, 3), (7, 1), (8, 2), (14, 2)])
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 def test_prefill_head_configs(attn, hq, hkv, d, prec):
     _check_prefill(attn, 300, hq, hkv, d, prec, seed=hq * 10 + hkv + d)
 
@@ -166,16 +167,18 @@ def test_prefill_fp32_every_query_block_size(attn, m, hq, hkv, d):
     _check_prefill(attn, m, hq, hkv, d, FP32, seed=m + hq + d)
 
 
-def test_prefill_long_sequence_sampled_rows(attn):
-    """32768 tokens over 2 query heads: query tiles walk up to 256 key tiles,
-    and the 256 CTAs take more than one wave on the SMs."""
+@pytest.mark.parametrize("prec", [FP16, TF32])
+def test_prefill_long_sequence_sampled_rows(attn, prec):
+    """32768 tokens over 2 query heads: query tiles walk up to 256 key tiles
+    of 128 keys (512 of 64 keys in the TF32 mode), and the 256 CTAs take more
+    than one wave on the SMs."""
     m, hq, hkv, d = 32768, 2, 1, 128
     rows = workloads.sample_rows(m, 321, n_random=128)
-    amax, _ = _check_prefill(attn, m, hq, hkv, d, FP16, seed=321, rows=rows)
+    amax, _ = _check_prefill(attn, m, hq, hkv, d, prec, seed=321, rows=rows)
     print(f"prefill m={m}: {len(rows)} rows, max abs {amax:.3e}")
 
 
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 def test_prefill_sharp_softmax(attn, prec):
     """scale 2 on N(0,1) inputs (head_dim 128): scores spread over about
     +-100 in log2 units, so the running max moves past the rescale threshold
@@ -203,23 +206,24 @@ def test_decode_sharp_softmax(attn):
     assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
 
 
-def test_prefill_split_into_many_key_chunks(attn):
+@pytest.mark.parametrize("prec", [FP16, TF32])
+def test_prefill_split_into_many_key_chunks(attn, prec):
     """4096 tokens over 2 query heads leave most SMs idle, so the key walk of
-    each query-tile pair is split into 4-tile chunks: up to 8 chunk partials
-    per row, more than one batch of the combine.  Sampled rows include the
-    first and last tiles."""
+    each query-tile pair is split into chunks of four 128-key blocks: up to 8
+    chunk partials per row, more than one batch of the combine.  Sampled rows
+    include the first and last tiles."""
     m, hq, hkv, d = 4096, 2, 1, 64
     rows = workloads.sample_rows(m, 91)
-    amax, _ = _check_prefill(attn, m, hq, hkv, d, FP16, seed=91, rows=rows)
+    amax, _ = _check_prefill(attn, m, hq, hkv, d, prec, seed=91, rows=rows)
     print(f"split prefill m={m}: {len(rows)} rows, max abs {amax:.3e}")
 
 
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 def test_prefill_padded_strides(attn, prec):
     _check_prefill(attn, 333, 6, 2, 128, prec, seed=7, q_pad=64, kv_pad=128)
 
 
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 @pytest.mark.parametrize("d", [64, 128])
 def test_prefill_stride_padding_is_never_read(attn, prec, d):
     """NaN in the padding columns between rows (past Hq*D in Q, past Hkv*D in
@@ -240,7 +244,7 @@ def test_prefill_stride_padding_is_never_read(attn, prec, d):
         assert amax <= TC_ABS, amax
 
 
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 def test_prefill_single_packed_buffer(attn, prec):
     """Q, K, V as column slices of one [M, (Hq+2Hkv)D] projection output with
     equal strides (the page's zero-copy packed layout)."""
@@ -262,7 +266,7 @@ def test_prefill_single_packed_buffer(attn, prec):
     assert amax <= (FP32_ABS if prec == FP32 else TC_ABS)
 
 
-@pytest.mark.parametrize("prec", [FP16, FP32])
+@pytest.mark.parametrize("prec", [FP16, TF32, FP32])
 def test_prefill_explicit_scale(attn, prec):
     m, hq, hkv, d = 150, 2, 1, 64
     qs, kvs = hq * d, hkv * d
@@ -278,7 +282,7 @@ def test_prefill_rows_beyond_m_untouched(attn):
     m, hq, hkv, d = 130, 2, 2, 128
     qs = hq * d
     q, k, v = workloads.prefill_inputs(m, qs, hkv * d, 3)
-    for prec in (FP16, FP32):
+    for prec in (FP16, TF32, FP32):
         buf, o = guarded_empty((m + 126) * qs)
         attn.attn_prefill_causal(q.cuda(), k.cuda(), v.cuda(), o, m, hq, hkv, d, qs, hkv * d,
                                  precision=prec)
@@ -662,7 +666,8 @@ def test_prefill_fp32_waits_for_the_kernel_before_it(attn):
         assert amax <= FP32_ABS and rel <= FP32_REL, (amax, rel)
 
 
-def test_prefill_tc_waits_for_the_kernels_before_it(attn):
+@pytest.mark.parametrize("prec", [FP16, TF32])
+def test_prefill_tc_waits_for_the_kernels_before_it(attn, prec):
     """The tensor-core prefill chains its kernels as programmatic dependents
     (rounding pre-pass, main kernel staging the caller's Q before it waits
     for the pre-pass, combine), and its pre-pass depends the same way on the
@@ -677,11 +682,11 @@ def test_prefill_tc_waits_for_the_kernels_before_it(attn):
     dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
     outs = [torch.full((m, qs), float("nan"), device="cuda") for _ in range(3)]
     torch.cuda.synchronize()
-    attn.attn_prefill_causal(dq, dk, dv, outs[0], m, hq, hkv, d, qs, kvs)
+    attn.attn_prefill_causal(dq, dk, dv, outs[0], m, hq, hkv, d, qs, kvs, precision=prec)
     dk.copy_(k2.cuda())                # predecessor kernels of the next call
     dv.copy_(v2.cuda())
-    attn.attn_prefill_causal(dq, dk, dv, outs[1], m, hq, hkv, d, qs, kvs)
-    attn.attn_prefill_causal(outs[1], dk, dv, outs[2], m, hq, hkv, d, qs, kvs)
+    attn.attn_prefill_causal(dq, dk, dv, outs[1], m, hq, hkv, d, qs, kvs, precision=prec)
+    attn.attn_prefill_causal(outs[1], dk, dv, outs[2], m, hq, hkv, d, qs, kvs, precision=prec)
     torch.cuda.synchronize()
     assert attn.attn_get_device_status() == attn.ATTN_OK
     rows = workloads.sample_rows(m, 5, 16, 16, 48)
@@ -712,7 +717,7 @@ def test_decode_workspace_reuse(attn):
 
 # ------------------------------------------------------------------ autoregressive loop
 
-@pytest.mark.parametrize("prec", [FP32, FP16])
+@pytest.mark.parametrize("prec", [FP32, FP16, TF32])
 def test_autoregressive_steps_match_prefill_rows(attn, prec):
     """Prefill a prompt, then run decode steps that append each new token's
     K/V row and attend to the cache: step t must reproduce row P+t of a causal
@@ -767,3 +772,26 @@ def test_prefill_bf16_operands(attn, m, hq, hkv, d):
     assert amax <= 2.5e-2, amax
     got16 = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, FP16)
     assert compare(got16, ref)[0] <= TC_ABS
+
+
+# ------------------------------------------------------------------ TF32 operand mode
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_tf32_takes_inputs_beyond_the_fp16_range(attn, d):
+    """ATTN_PREC_TF32 keeps fp32's exponent: Q scaled by 1e5 (past fp16's
+    65504), K by 1e-5 (below fp16's normal range) and V by 1e5.  The scores
+    are those of the unscaled inputs, the output is 1e5 times theirs, and the
+    TF32 result meets the tensor-core bound after dividing by 1e5.  The fp16
+    mode flags the same inputs with ATTN_ERR_RANGE."""
+    m, hq, hkv = 300, 4, 2
+    qs, kvs = hq * d, hkv * d
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, 202)
+    q, k, v = q * 1e5, k * 1e-5, v * 1e5
+    got = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, TF32)
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs)
+    amax, _ = compare(got / 1e5, ref / 1e5)
+    assert amax <= TC_ABS, amax
+    buf, o = guarded_empty(m * qs)
+    attn.attn_prefill_causal(q.cuda(), k.cuda(), v.cuda(), o, m, hq, hkv, d, qs, kvs,
+                             precision=FP16)
+    assert attn.attn_get_device_status() == attn.ATTN_ERR_RANGE
