@@ -293,6 +293,11 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc_fence_after();
                 bool k_next_ready = false;
                 const uint32_t jn = j + 1;
+                // V(j)'s slot is released as soon as its last P.V MMA is
+                // issued (its commit completes with that MMA), so that the
+                // K tile two steps ahead, which reuses the slot, loads during
+                // the following S MMA rather than after it.
+                const int last_pv = j < tile_n[1] ? 1 : 0;
                 for (int t = 0; t < kNQ && ok; ++t) {
                     if (j < tile_n[t]) {
                         ok = mbar_wait(smem_u32(&bars.p_full[t]), j & 1, wait_ns, status, kStatusTimeout);
@@ -300,6 +305,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         tc_fence_after();
                         issue_pv(t, j);
                     }
+                    if (t == last_pv) mma_commit(smem_u32(&bars.empty[(2 * j + 1) % kSlots]));
                     if (jn < tile_n[t]) {
                         if (!k_next_ready) {
                             ok = wait_load(2 * jn);
@@ -311,7 +317,6 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&bars.empty[(2 * j + 1) % kSlots]));
                 if (k_next_ready) mma_commit(smem_u32(&bars.empty[(2 * jn) % kSlots]));
             }
             if (!ok) record_timeout(status, &bars);
