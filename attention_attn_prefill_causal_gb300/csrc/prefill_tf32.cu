@@ -12,9 +12,11 @@
 // (the low 13 mantissa bits are dropped).  Q goes to the tensor core as the
 // caller stored it.  K and V are rounded to nearest TF32 by a pre-pass: an
 // operand dropped toward zero would bias the output (O = V[0] exactly for
-// row 0), which rounding to nearest halves and unbiases.  P is written as
-// fp32 and its low bits are dropped by the MMA; the row sum is taken from
-// the fp32 weights.
+// row 0), which rounding to nearest halves and unbiases.  P is truncated to
+// TF32 by the softmax itself and the row sum is taken over the truncated
+// weights, so the weights the MMA applies are normalised exactly (a row sum
+// over the untruncated weights would scale every output down by up to
+// 2^-10 where the running max lags the row's largest score).
 //
 // Layout.  The pre-pass writes K rounded, [m, kv_heads*D] fp32, and V
 // rounded and transposed per KV head, [kv_heads*D, m4] fp32 (keys
@@ -68,6 +70,7 @@ constexpr int kSlots = 3;              // operand ring slots
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // the bits of an fp32 a TF32 operand keeps
 
 template <int D>
 struct Tf32Layout {
@@ -384,10 +387,15 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int i = 0; i < 16; ++i) {
                     const float2 x = __ffma2_rn(
                         make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2, nm2);
-                    const float p0 = ex2(x.x), p1 = ex2(x.y);
-                    acc[i % 4] = __fadd2_rn(acc[i % 4], make_float2(p0, p1));
-                    pk[2 * i] = __float_as_uint(p0);
-                    pk[2 * i + 1] = __float_as_uint(p1);
+                    // The MMA reads the weights' top 19 bits; the row sum takes
+                    // the same truncated values, so the output is an exact
+                    // convex combination of the weights the MMA used.
+                    const uint32_t b0 = __float_as_uint(ex2(x.x)) & kTf32Mask;
+                    const uint32_t b1 = __float_as_uint(ex2(x.y)) & kTf32Mask;
+                    acc[i % 4] = __fadd2_rn(acc[i % 4],
+                                            make_float2(__uint_as_float(b0), __uint_as_float(b1)));
+                    pk[2 * i] = b0;
+                    pk[2 * i + 1] = b1;
                 }
                 tmem_st32(t_s + c * 32, pk);
             }
