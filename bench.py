@@ -325,6 +325,26 @@ def remainder_graphs(bench, stream, append=True):
 TF32_PEAK_RATIO = 1.1 / 2.25
 
 
+def prefill_launches(m, num_q_heads, sms):
+    """Kernels one tensor-core prefill call launches: the rounding pre-pass
+    and the main kernel, plus the combine kernel when the call splits its key
+    walk.  Mirrors the library's split plan: split only when query-tile pairs
+    x heads leave SMs idle, with the smallest chunk whose items fit in one
+    wave."""
+    n_qt = -(-m // 128)
+    n_pairs = -(-m // 256)
+
+    def nk(pr):
+        return min(2 * pr + 2, n_qt)
+    if n_pairs == 0 or n_pairs * num_q_heads >= sms:
+        return 2
+    nk_last = nk(n_pairs - 1)
+    for c in range(2, nk_last):
+        if sum(-(-nk(pr) // c) for pr in range(n_pairs)) * num_q_heads <= sms:
+            return 3
+    return 2
+
+
 class PrefillBench:
     def __init__(self, attn, shape, device, precision=None):
         self.attn, self.c, self.dev = attn, shape, device
@@ -343,10 +363,8 @@ class PrefillBench:
         # The workspace holds the rounded K and V (two 256-byte aligned
         # matrices of 2 bytes per element, 4 in the TF32 mode) and, when the
         # call splits its key walk, the partials that a third kernel merges.
-        esize = 4 if self.prec == attn.ATTN_PREC_TF32 else 2
-        kv_bytes = shape.m * shape.num_kv_heads * shape.head_dim * esize
-        operands = 2 * ((kv_bytes + 255) // 256 * 256)
-        self.launches_per_call = 3 if ws > operands + 512 else 2
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.launches_per_call = prefill_launches(shape.m, shape.num_q_heads, sms)
 
     def call(self, i, stream):
         c, a, r = self.c, self.attn, i % self.R
