@@ -390,41 +390,10 @@ class PrefillBench:
         return float(np.abs(got - ref).max())
 
 
-def bench_prefill_tf32(attn, shape, device, stream, calls, peaks, peak_src):
-    """The TF32 mode on a prefill workload: device time per call and its
-    fraction of the TF32 dense peak (no end-to-end leg)."""
-    pb = PrefillBench(attn, shape, device, attn.ATTN_PREC_TF32)
-    err = pb.check()
-
-    def chunk():
-        for i in range(pb.R):
-            pb.call(i, stream)
-    g = make_graph(chunk, stream)
-    for _ in range(2):
-        g.replay()
-    torch.cuda.synchronize()
-    reps = max(1, math.ceil(calls / pb.R))
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(reps):
-            g.replay()
-        end.record(stream)
-    end.synchronize()
-    secs = start.elapsed_time(end) / 1e3
-    per_call = secs / (reps * pb.R)
-    tflops = shape.flops() / per_call / 1e12
-    peak_key = "bf16_tflops_sustained" if secs > 1.0 else "bf16_tflops"
-    peak = float(peaks[peak_key]) * TF32_PEAK_RATIO
-    return {"value": round(tflops, 2), "unit": "TFLOP/s", "us": round(per_call * 1e6, 2),
-            "frac": round(tflops / peak, 4), "peak": round(peak, 1), "err": float(f"{err:.3g}"),
-            "launches": pb.launches_per_call}
-
-
-def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
-    pb = PrefillBench(attn, shape, device)
-    err = pb.check()
-
+def time_prefill_calls(pb, stream, calls):
+    """Device seconds per call of a prefill workload: CUDA-graph replays of
+    one call per input replica (after two warm-up replays), CUDA events on
+    the launching stream.  Returns (seconds per call, calls, total seconds)."""
     def chunk():
         for i in range(pb.R):
             pb.call(i, stream)
@@ -442,7 +411,27 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
     end.synchronize()
     secs = start.elapsed_time(end) / 1e3
     n = reps * pb.R
-    per_call = secs / n
+    return secs / n, n, secs
+
+
+def bench_prefill_tf32(attn, shape, device, stream, calls, peaks, peak_src):
+    """The TF32 mode on a prefill workload: device time per call and its
+    fraction of the TF32 dense peak (no end-to-end leg)."""
+    pb = PrefillBench(attn, shape, device, attn.ATTN_PREC_TF32)
+    err = pb.check()
+    per_call, _, secs = time_prefill_calls(pb, stream, calls)
+    tflops = shape.flops() / per_call / 1e12
+    peak_key = "bf16_tflops_sustained" if secs > 1.0 else "bf16_tflops"
+    peak = float(peaks[peak_key]) * TF32_PEAK_RATIO
+    return {"value": round(tflops, 2), "unit": "TFLOP/s", "us": round(per_call * 1e6, 2),
+            "frac": round(tflops / peak, 4), "peak": round(peak, 1), "err": float(f"{err:.3g}"),
+            "launches": pb.launches_per_call}
+
+
+def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
+    pb = PrefillBench(attn, shape, device)
+    err = pb.check()
+    per_call, n, secs = time_prefill_calls(pb, stream, calls)
     flops = shape.flops()
     tflops = flops / per_call / 1e12
     peak_key = "bf16_tflops_sustained" if secs > 1.0 else "bf16_tflops"
