@@ -80,3 +80,20 @@ def test_traffic_hash_ignores_comments_only():
     changed = "int f(int x) {  // doubles x\n    return 3 * x;\n}\n"
     assert bench.code_text(src) == bench.code_text(same) == "int f(int x) { return 2 * x; }"
     assert bench.code_text(changed) != bench.code_text(src)
+
+
+@pytest.mark.parametrize("m,hq,hkv,d", [(2048, 12, 2, 128), (16384, 28, 4, 128), (4096, 2, 1, 64),
+                                        (300, 4, 2, 128), (1000, 40, 8, 64), (5000, 3, 1, 128)])
+def test_prefill_launch_count_follows_the_library_plan(m, hq, hkv, d):
+    """bench.py counts a third launch (the combine kernel) exactly when the
+    library splits the key walk, which shows in the workspace as chunk
+    partials beyond the rounded K and V (both sizes are host arithmetic over
+    152 SMs when no GPU is visible)."""
+    import attention_attn_prefill_causal_gb300 as attn
+    ws16 = attn.attn_prefill_workspace_size(m, hq, hkv, d, attn.ATTN_PREC_FP16)
+    operands16 = 2 * (-(-m * hkv * d * 2 // 256) * 256)
+    wst = attn.attn_prefill_workspace_size(m, hq, hkv, d, attn.ATTN_PREC_TF32)
+    operandst = -(-m * hkv * d * 4 // 256) * 256 + -(-hkv * d * (-(-m // 4) * 4) * 4 // 256) * 256
+    launches = bench.prefill_launches(m, hq, 152)
+    assert (ws16 > operands16) == (launches == 3), (ws16, operands16, launches)
+    assert (wst > operandst) == (launches == 3), (wst, operandst, launches)
