@@ -660,7 +660,7 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
                       uint32_t kv_stride, float scale, void* workspace, unsigned int* status,
                       uint64_t wait_ns, cudaStream_t stream) {
     using L = TcLayout<D>;
-    const PrefillPlan plan = make_plan(m, num_q_heads, D, device_sm_count(), 1);
+    const PrefillPlan plan = make_plan(m, num_q_heads, D, device_sm_count(), 1, kNQ);
     const size_t operand_bytes = operand_bytes_16(m, num_kv_heads, D);
     const uint32_t q_cols = num_q_heads * D, kv_cols = num_kv_heads * D;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -734,7 +734,7 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
 
 size_t prefill_tc_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim) {
-    const PrefillPlan p = make_plan(m, num_q_heads, head_dim, device_sm_count(), 1);
+    const PrefillPlan p = make_plan(m, num_q_heads, head_dim, device_sm_count(), 1, kNQ);
     return operand_bytes_16(m, num_kv_heads, head_dim) + p.part_o_bytes + p.part_ml_bytes;
 }
 

@@ -170,35 +170,37 @@ struct PrefillPlan {
     size_t part_o_bytes, part_ml_bytes;
 };
 
-// Split the KV walk only when the pairs alone leave SMs idle: then take the
-// smallest chunk (most parallelism, shortest item) whose items still fit in
-// one wave.  Chunks are counted in 128-key blocks (nk(p) = blocks of pair
-// p's second tile) and converted to key tiles of 128 / kv_per_qtile keys.
+// Split the KV walk only when the work items alone leave SMs idle: then
+// take the smallest chunk (most parallelism, shortest item) whose items still
+// fit in one wave.  A work item is `tiles_per_item` consecutive query tiles
+// (a pair in the 16-bit kernel, one tile in the TF32 kernel); chunks are
+// counted in 128-key blocks (nk(u) = blocks of item u's last tile) and
+// converted to key tiles of 128 / kv_per_qtile keys.
 PrefillPlan make_plan(uint32_t m, uint32_t num_q_heads, uint32_t head_dim, int sm_count,
-                      uint32_t kv_per_qtile) {
+                      uint32_t kv_per_qtile, uint32_t tiles_per_item) {
     PrefillPlan p{};
     const uint32_t n_qt = (m + kBM - 1) / kBM;
-    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
-    auto nk = [&](uint32_t pr) { return std::min(kNQ * pr + kNQ, n_qt); };
-    p.n_items = n_pairs;
+    const uint32_t n_units = (m + tiles_per_item * kBM - 1) / (tiles_per_item * kBM);
+    auto nk = [&](uint32_t u) { return std::min(tiles_per_item * u + tiles_per_item, n_qt); };
+    p.n_items = n_units;
     p.split.kv_chunk = kNoSplit;
     p.split.n_chunks_max = 1;
     p.split.first_split_row = m;
     p.split.m_pad = n_qt * kBM;
     p.split.kv_per_qtile = kv_per_qtile;
     const uint32_t sms = (uint32_t)std::max(sm_count, 1);
-    if (n_pairs > 0 && (uint64_t)n_pairs * num_q_heads < sms) {
-        const uint32_t nk_last = nk(n_pairs - 1);
+    if (n_units > 0 && (uint64_t)n_units * num_q_heads < sms) {
+        const uint32_t nk_last = nk(n_units - 1);
         for (uint32_t c = 2; c < nk_last; ++c) {
             uint32_t items = 0;
-            for (uint32_t pr = 0; pr < n_pairs; ++pr) items += (nk(pr) + c - 1) / c;
+            for (uint32_t u = 0; u < n_units; ++u) items += (nk(u) + c - 1) / c;
             if ((uint64_t)items * num_q_heads <= sms) {
                 p.n_items = items;
                 p.split.kv_chunk = c * kv_per_qtile;
                 p.split.n_chunks_max = (nk_last + c - 1) / c;
                 uint32_t first = 0;
-                while (first < n_pairs && nk(first) <= c) ++first;
-                p.split.first_split_row = std::min(m, first * kNQ * kBM);
+                while (first < n_units && nk(first) <= c) ++first;
+                p.split.first_split_row = std::min(m, first * tiles_per_item * kBM);
                 break;
             }
         }

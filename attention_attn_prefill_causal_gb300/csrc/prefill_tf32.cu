@@ -21,26 +21,29 @@
 // Layout.  The pre-pass writes K rounded, [m, kv_heads*D] fp32, and V
 // rounded and transposed per KV head, [kv_heads*D, m4] fp32 (keys
 // contiguous, m4 = m rounded up to 4), so that both MMAs read K-major
-// operands in the 128-byte swizzled layout TMA writes: S = Q K^T takes Q
-// (128 rows x D) and a K tile (64 keys x D); O += P V takes P from TMEM
-// (128 rows x 64 keys, one fp32 per column) and a V^T tile (D rows x 64
-// keys).
+// operands in the 128-byte swizzled layout TMA writes.
 //
-// CTA work unit: two consecutive 128-row query tiles of one head (as in the
-// 16-bit kernel), keys walked in 64-key tiles up to the diagonal.  Shared
-// memory holds both fp32 query tiles (2 x 64 KB at D = 128) and a ring of
-// three 32 KB slots that K tiles and V^T tiles pass through in load order
-// K(0), V(0), K(1), V(1), ...; a K tile is freed when both query tiles'
-// S MMAs of it completed, a V^T tile when both P.V MMAs did.  Warp roles
-// (320 threads): warps 0-3 softmax for tile A, 4-7 for tile B (thread =
-// TMEM lane = query row), warp 8 TMA producer, warp 9 TMEM allocator and
-// MMA issuer.  TMEM per tile: S/P in 64 columns and O in D columns.  The MMA
-// thread ping-pongs the tiles exactly as the 16-bit kernel does.
-// Epilogue: after the CTA's last MMA the query tiles are dead; each softmax
-// thread writes its row of O into the 128-byte swizzled boxes that held its
-// tile's Q, and one thread per tile stores them with TMA.
-// Small grids split each pair's key walk into chunks of whole 128-key
-// blocks, merged by the combine kernel shared with the 16-bit path.
+// CTA work unit: one 128-row query tile of one head; keys are walked in
+// 128-key steps up to the diagonal.  TF32 MMAs run at half the 16-bit rate,
+// so one tile's own MMAs (S = Q K^T and O += P V, about 1 us per step) last
+// longer than its softmax; with S double-buffered in TMEM the tensor core
+// computes S(j+1) and P(j-1).V while the softmax works on S(j), and a single
+// tile keeps it busy.  TMEM (512 columns): S/P buffers 0 and 1 (128 columns
+// each), O (D columns) and the query tile (D columns; the S MMA takes A from
+// TMEM).  Shared memory holds only a ring of seven 32 KB slots: a 128-key K
+// tile is D/64 slots (64 of its D columns each) and a V^T tile D/64 slots
+// (128*64/D keys each), loaded in the order the MMAs consume them:
+// K(0), K(1), V(0), K(2), V(1), K(3), ...  The MMA thread issues S(0), S(1),
+// then per step j: P(j).V, then S(j+2) into the buffer P(j) occupied (MMAs
+// execute in issue order, so S(j+2) overwrites P(j) after P(j).V has read
+// it).  A slot is released by a commit right after the MMAs that read it.
+// Warp roles (192 threads): warps 0-3 softmax (thread = TMEM lane = query
+// row), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer.
+// The softmax rescales O only when the running max grows by more than 8
+// (log2 units); it then first waits for the previous P.V (O stable).
+// Epilogue: O (normalised, or a chunk's unnormalised partial) into the ring's
+// first slots, then TMA stores.  Small grids split each tile's key walk into
+// chunks merged by the combine kernel shared with the 16-bit path.
 // Launch chain (programmatic dependent launches): the pre-pass waits for the
 // kernel before the call, then lets this kernel launch; this kernel stages
 // the caller's Q at once and waits for the pre-pass before its first K/V
@@ -64,40 +67,48 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBK = 64;                // keys per key tile
-constexpr uint32_t kPerQ = kBM / kBK;  // key tiles per 128-key block
-constexpr int kSlots = 3;              // operand ring slots
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kBK = 128;               // keys per step
+constexpr uint32_t kPerQ = kBM / kBK;  // key tiles per 128-key block (1)
+constexpr int kSlots = 7;              // operand ring slots
+constexpr uint32_t kSlotBytes = 32 * 1024;
+constexpr int kSoftmaxThreads = 128;   // warps 0-3
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // the bits of an fp32 a TF32 operand keeps
 
 template <int D>
 struct Tf32Layout {
+    static constexpr int kPieces = D / 64;                      // slots per K or V^T tile
     static constexpr uint32_t kQBoxBytes = kBM * 128;           // 128 rows x 32 floats
-    static constexpr uint32_t kQTileBytes = kBM * D * 4;        // D/32 boxes
-    static constexpr uint32_t kKBoxBytes = kBK * 128;           // 64 keys x 32 floats
+    static constexpr uint32_t kKBoxBytes = kBK * 128;           // 128 keys x 32 floats
     static constexpr uint32_t kVBoxBytes = D * 128;             // D rows x 32 keys
-    static constexpr uint32_t kSlotBytes = kBK * D * 4;         // one K or V^T tile
-    static constexpr uint32_t kQOff = 0;
-    static constexpr uint32_t kRingOff = kNQ * kQTileBytes;
-    static constexpr uint32_t kBytes = kRingOff + kSlots * kSlotBytes;
+    static constexpr int kKBoxesPerPiece = 2;                   // 64 columns of K
+    static constexpr int kVBoxesPerPiece = 4 / kPieces;         // 128 / kPieces keys of V^T
+    static constexpr int kVStepsPerPiece = kBK / 8 / kPieces;   // P.V MMAs (8 keys) per piece
+    static constexpr uint32_t kTileBytes = kBM * D * 4;         // a query or output tile
+    static constexpr int kQSlots = kTileBytes / kSlotBytes;     // query staging / O staging
+    static constexpr int kQStageSlot = kSlots - kQSlots;
+    static constexpr uint32_t kBytes = kSlots * kSlotBytes;
     static constexpr uint32_t kSmemAlloc = kBytes + 1024;       // room to align to 1 KB
-    static constexpr uint32_t kTileCols = D == 128 ? 256 : 128; // TMEM columns per tile
-    static constexpr uint32_t kOCol = D == 128 ? 128 : 64;      // O's first column in a tile
-    static constexpr uint32_t kTmemCols = kNQ * kTileCols;
-    static_assert(kBK + D <= kTileCols && kOCol >= kBK, "TMEM tile layout");
+    static constexpr uint32_t kOCol = 2 * kBK;                  // TMEM: S0 | S1 | O | Q
+    static constexpr uint32_t kQCol = kOCol + D;
+    static_assert(kQCol + D <= kTmemCols, "TMEM layout");
+    static_assert(kKBoxesPerPiece * kKBoxBytes == kSlotBytes, "K piece");
+    static_assert(kVBoxesPerPiece * kVBoxBytes == kSlotBytes, "V piece");
+    static_assert(kQSlots * kSlotBytes == kTileBytes, "query staging");
     static_assert(kSmemAlloc <= 227 * 1024, "shared memory");
-    // O staging (fp32, the same box layout as Q) reuses the query tiles.
-    static_assert(kQTileBytes == kBM * D * 4, "O staging");
 };
 
 struct __align__(8) Tf32Barriers {
-    uint64_t q_full[kNQ];
+    uint64_t q_full;        // the fp32 query tile landed in the staging slots
+    uint64_t q_ready;       // the query tile is in TMEM (every softmax thread arrives)
     uint64_t full[kSlots];
     uint64_t empty[kSlots];
-    uint64_t s_full[kNQ];
-    uint64_t p_full[kNQ];
+    uint64_t s_full[2];     // S(j) in buffer j % 2 computed
+    uint64_t p_full[2];     // P(j) in buffer j % 2 written
+    uint64_t pv_last;       // P.V of the second-to-last step completed (one phase)
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort;
@@ -123,21 +134,19 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __shared__ Tf32Barriers bars;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
+    const uint32_t n_qt = (m + kBM - 1) / kBM;
     const uint32_t h = blockIdx.x % num_q_heads;
     const uint32_t kvh = h / heads_per_kv;
-    // Work item: (query-tile pair, key chunk), heaviest pairs first.
-    uint32_t pair = 0, chunk = 0, n_chunks = 1;
+    // Work item: (query tile, key chunk), heaviest tiles first.
+    uint32_t qt = 0, chunk = 0, n_chunks = 1;
     if (split.kv_chunk == kNoSplit) {
-        pair = n_pairs - 1 - blockIdx.x / num_q_heads;
+        qt = n_qt - 1 - blockIdx.x / num_q_heads;
     } else {
         uint32_t idx = blockIdx.x / num_q_heads;
-        for (int p = (int)n_pairs - 1; p >= 0; --p) {
-            const uint32_t nk = max(kv_tiles_for(p * kNQ, m, kPerQ),
-                                    kv_tiles_for(p * kNQ + 1, m, kPerQ));
-            const uint32_t nc = (nk + split.kv_chunk - 1) / split.kv_chunk;
+        for (int t = (int)n_qt - 1; t >= 0; --t) {
+            const uint32_t nc = (kv_tiles_for(t, m, kPerQ) + split.kv_chunk - 1) / split.kv_chunk;
             if (idx < nc) {
-                pair = (uint32_t)p;
+                qt = (uint32_t)t;
                 chunk = idx;
                 n_chunks = nc;
                 break;
@@ -145,35 +154,27 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             idx -= nc;
         }
     }
-    const uint32_t qt0 = pair * kNQ;
-    uint32_t n_kv[kNQ];
-#pragma unroll
-    for (int t = 0; t < kNQ; ++t) n_kv[t] = kv_tiles_for(qt0 + t, m, kPerQ);
-    uint32_t n_kv_pair = 0;
-#pragma unroll
-    for (int t = 0; t < kNQ; ++t) n_kv_pair = max(n_kv_pair, n_kv[t]);
-    // This item's key tiles are [j0, j0 + n_kv_all); tile t takes the first
-    // tile_n[t] of them.
+    const uint32_t n_kv_tile = kv_tiles_for(qt, m, kPerQ);
+    // This item's key steps are [j0, j0 + nkv).
     const uint32_t j0 = split.kv_chunk == kNoSplit ? 0u : chunk * split.kv_chunk;
-    const uint32_t n_kv_all =
-        split.kv_chunk == kNoSplit ? n_kv_pair : min(n_kv_pair, j0 + split.kv_chunk) - j0;
-    uint32_t tile_n[kNQ];
-#pragma unroll
-    for (int t = 0; t < kNQ; ++t) tile_n[t] = n_kv[t] > j0 ? min(n_kv[t] - j0, n_kv_all) : 0;
+    const uint32_t nkv =
+        split.kv_chunk == kNoSplit ? n_kv_tile : min(n_kv_tile, j0 + split.kv_chunk) - j0;
+    const uint32_t tile_row0 = qt * kBM;
 
-    const uint32_t sQ = smem_u32(smem + L::kQOff);
-    const uint32_t sR = smem_u32(smem + L::kRingOff);
+    const uint32_t sR = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int t = 0; t < kNQ; ++t) {
-            mbar_init(smem_u32(&bars.q_full[t]), 1);
-            mbar_init(smem_u32(&bars.s_full[t]), 1);
-            mbar_init(smem_u32(&bars.p_full[t]), kBM);
-        }
+        mbar_init(smem_u32(&bars.q_full), 1);
+        mbar_init(smem_u32(&bars.q_ready), kSoftmaxThreads);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(smem_u32(&bars.full[s]), 1);
             mbar_init(smem_u32(&bars.empty[s]), 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars.s_full[b]), 1);
+            mbar_init(smem_u32(&bars.p_full[b]), kSoftmaxThreads);
+        }
+        mbar_init(smem_u32(&bars.pv_last), 1);
         mbar_init(smem_u32(&bars.mma_done), 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -181,7 +182,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(&bars.tmem_base), L::kTmemCols);
+        tmem_alloc(smem_u32(&bars.tmem_base), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -189,25 +190,43 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
+    // Loads of the item, in the order the MMAs consume them: K(0), K(1),
+    // then V(i) and K(i + 2) alternately.  Unit u is one tile; load n is
+    // piece n % kPieces of unit n / kPieces.
+    const uint32_t n_units = nkv > 0 ? 2 * nkv : 0;
+    auto unit_of = [&](uint32_t u, bool& is_k, uint32_t& step) {
+        if (u < 2 && u < nkv) { is_k = true; step = u; return; }
+        // after K(0) and K(1): V(i) at 2 + 2i (with K(i+2) at 3 + 2i while i + 2 < nkv);
+        // once the keys run out, the remaining units are V tiles only
+        const uint32_t first_v = nkv < 2 ? nkv : 2u;
+        const uint32_t r = u - first_v;
+        const uint32_t paired = nkv > 2 ? nkv - 2 : 0u;  // V(i) followed by K(i+2) for i < paired
+        if (r < 2 * paired) {
+            is_k = (r & 1u) != 0;
+            step = is_k ? r / 2 + 2 : r / 2;
+        } else {
+            is_k = false;
+            step = paired + (r - 2 * paired);
+        }
+    };
+
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_vt);
-            for (int t = 0; t < kNQ; ++t) {
-                const uint32_t bar = smem_u32(&bars.q_full[t]);
-                mbar_arrive_expect_tx(bar, L::kQTileBytes);
+            {
+                const uint32_t bar = smem_u32(&bars.q_full);
+                mbar_arrive_expect_tx(bar, L::kTileBytes);
                 for (uint32_t b = 0; b < D / 32; ++b)
-                    tma_load_2d(sQ + t * L::kQTileBytes + b * L::kQBoxBytes, &tm_q, bar,
-                                (int32_t)(h * D + b * 32), (int32_t)((qt0 + t) * kBM));
+                    tma_load_2d(sR + L::kQStageSlot * kSlotBytes + b * L::kQBoxBytes, &tm_q, bar,
+                                (int32_t)(h * D + b * 32), (int32_t)tile_row0);
             }
             // K and V^T come from the pre-pass: read them only once its grid
             // (and with it every kernel before the call) has completed.
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            // Load n of the item: K(n/2) for even n, V^T(n/2) for odd n, into
-            // slot n % kSlots (use n / kSlots of that slot).
-            const uint32_t n_loads = 2 * n_kv_all;
+            const uint32_t n_loads = n_units * L::kPieces;
             uint32_t issued = 0;
             bool ok = true;
             for (uint32_t n = 0; n < n_loads; ++n) {
@@ -215,26 +234,35 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (use > 0) {
                     ok = mbar_wait(smem_u32(&bars.empty[slot]), (use - 1) & 1, wait_ns, status,
                                    kStatusTimeout);
-                    if (!ok) break;
+                } else if (slot >= (uint32_t)L::kQStageSlot) {
+                    // the query staging slots are free once the tile is in TMEM
+                    ok = mbar_wait(smem_u32(&bars.q_ready), 0, wait_ns, status, kStatusTimeout);
                 }
+                if (!ok) break;
+                bool is_k;
+                uint32_t step;
+                unit_of(n / L::kPieces, is_k, step);
+                const uint32_t piece = n % L::kPieces;
                 const uint32_t bar = smem_u32(&bars.full[slot]);
-                const uint32_t dst = sR + slot * L::kSlotBytes;
-                const uint32_t key0 = (j0 + n / 2) * kBK;
-                mbar_arrive_expect_tx(bar, L::kSlotBytes);
-                if ((n & 1) == 0) {
-                    for (uint32_t b = 0; b < D / 32; ++b)
-                        tma_load_2d(dst + b * L::kKBoxBytes, &tm_k, bar, (int32_t)(kvh * D + b * 32),
+                const uint32_t dst = sR + slot * kSlotBytes;
+                const uint32_t key0 = (j0 + step) * kBK;
+                mbar_arrive_expect_tx(bar, kSlotBytes);
+                if (is_k) {
+                    for (int b = 0; b < L::kKBoxesPerPiece; ++b)
+                        tma_load_2d(dst + b * L::kKBoxBytes, &tm_k, bar,
+                                    (int32_t)(kvh * D + (piece * L::kKBoxesPerPiece + b) * 32),
                                     (int32_t)key0);
                 } else {
-                    for (uint32_t b = 0; b < kBK / 32; ++b)
-                        tma_load_2d(dst + b * L::kVBoxBytes, &tm_vt, bar, (int32_t)(key0 + b * 32),
+                    for (int b = 0; b < L::kVBoxesPerPiece; ++b)
+                        tma_load_2d(dst + b * L::kVBoxBytes, &tm_vt, bar,
+                                    (int32_t)(key0 + (piece * L::kVBoxesPerPiece + b) * 32),
                                     (int32_t)(kvh * D));
                 }
                 issued = n + 1;
             }
             if (!ok) record_timeout(status, &bars);
             // Drain: every copy this CTA issued must land before it exits.
-            for (int t = 0; t < kNQ; ++t) mbar_wait(smem_u32(&bars.q_full[t]), 0, kDrainWaitNs);
+            mbar_wait(smem_u32(&bars.q_full), 0, kDrainWaitNs);
             for (uint32_t n = (issued > kSlots ? issued - kSlots : 0); n < issued; ++n)
                 mbar_wait(smem_u32(&bars.full[n % kSlots]), (n / kSlots) & 1, kDrainWaitNs);
         }
@@ -243,84 +271,69 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_tf32(kBK, kBM);
             constexpr uint32_t idesc_pv = idesc_tf32(D, kBM);
-            bool ok = true;
-            for (int t = 0; t < kNQ && ok; ++t)
-                ok = mbar_wait(smem_u32(&bars.q_full[t]), 0, wait_ns, status, kStatusTimeout);
-            // Descriptor bases, built once; an operand at byte offset off in a
-            // tile is the base plus off >> 4.  K step ks (8 fp32 = 32 bytes)
-            // sits (ks % 4) * 32 bytes into a 128-byte swizzled row, in box ks / 4.
-            const uint64_t dq0 = smem_desc(sQ, 16, 1024, 2);
-            const uint64_t dq1 = smem_desc(sQ + L::kQTileBytes, 16, 1024, 2);
+            bool ok = nkv == 0 ||
+                      mbar_wait(smem_u32(&bars.q_ready), 0, wait_ns, status, kStatusTimeout);
+            // Slot descriptors: the ring's base plus slot * 32 KB (>> 4).  A
+            // K step of 8 fp32 (32 bytes) sits (ks % 4) * 32 bytes into a
+            // 128-byte swizzled row, in box ks / 4 of its piece.
             const uint64_t dr0 = smem_desc(sR, 16, 1024, 2);
-            auto slot_desc = [&](uint32_t n) {  // descriptor of load n's slot
-                return dr0 + (uint64_t)((n % kSlots) * (L::kSlotBytes / 16));
+            uint32_t load = 0;  // next load the MMAs consume
+            auto take = [&](uint64_t& desc, uint32_t& slot) {
+                slot = load % kSlots;
+                const bool got = mbar_wait(smem_u32(&bars.full[slot]), (load / kSlots) & 1, wait_ns,
+                                           status, kStatusTimeout);
+                desc = dr0 + (uint64_t)(slot * (kSlotBytes / 16));
+                ++load;
+                if (got) tc_fence_after();
+                return got;
             };
-            auto issue_s = [&](int t, uint32_t j) {
-                const uint64_t a0 = t == 0 ? dq0 : dq1;
-                const uint64_t b0 = slot_desc(2 * j);
-                const uint32_t d = tmem + t * L::kTileCols;
+            auto issue_s = [&](uint32_t j) {
+                const uint32_t d = tmem + (j & 1u) * kBK;
+                for (int p = 0; p < L::kPieces; ++p) {
+                    uint64_t b0;
+                    uint32_t slot;
+                    if (!take(b0, slot)) return false;
 #pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks) {
-                    const uint64_t offa = (uint64_t)((ks / 4) * (L::kQBoxBytes / 16) + (ks % 4) * 2);
-                    const uint64_t offb = (uint64_t)((ks / 4) * (L::kKBoxBytes / 16) + (ks % 4) * 2);
-                    mma_tf32_ss(d, a0 + offa, b0 + offb, idesc_s, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int k = p * 8 + ks;  // 8 of the D columns per MMA
+                        mma_tf32_ts(d, tmem + L::kQCol + k * 8,
+                                    b0 + (uint64_t)((ks / 4) * (L::kKBoxBytes / 16) + (ks % 4) * 2),
+                                    idesc_s, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&bars.empty[slot]));
                 }
-                mma_commit(smem_u32(&bars.s_full[t]));
+                mma_commit(smem_u32(&bars.s_full[j & 1u]));
+                return true;
             };
-            auto issue_pv = [&](int t, uint32_t j) {
-                const uint64_t b0 = slot_desc(2 * j + 1);
-                const uint32_t a = tmem + t * L::kTileCols, d = a + L::kOCol;
-                const uint32_t acc0 = j > 0 ? 1u : 0u;
+            auto issue_pv = [&](uint32_t j) {
+                const uint32_t a = tmem + (j & 1u) * kBK, d = tmem + L::kOCol;
+                for (int p = 0; p < L::kPieces; ++p) {
+                    uint64_t b0;
+                    uint32_t slot;
+                    if (!take(b0, slot)) return false;
 #pragma unroll
-                for (int ks = 0; ks < kBK / 8; ++ks)
-                    mma_tf32_ts(d, a + ks * 8,
-                                b0 + (uint64_t)((ks / 4) * (L::kVBoxBytes / 16) + (ks % 4) * 2),
-                                idesc_pv, ks > 0 ? 1u : acc0);
-            };
-            auto wait_load = [&](uint32_t n) {
-                return mbar_wait(smem_u32(&bars.full[n % kSlots]), (n / kSlots) & 1, wait_ns, status,
-                                 kStatusTimeout);
-            };
-            if (ok && n_kv_all > 0) {
-                ok = wait_load(0);
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < kNQ; ++t)
-                        if (tile_n[t] > 0) issue_s(t, 0);
-                    mma_commit(smem_u32(&bars.empty[0]));
+                    for (int ks = 0; ks < L::kVStepsPerPiece; ++ks) {
+                        const int k = p * L::kVStepsPerPiece + ks;  // 8 keys per MMA
+                        mma_tf32_ts(d, a + k * 8,
+                                    b0 + (uint64_t)((ks / 4) * (L::kVBoxBytes / 16) + (ks % 4) * 2),
+                                    idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&bars.empty[slot]));
                 }
-            }
-            for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
-                ok = wait_load(2 * j + 1);
+                // The last step's softmax rescales O only after this group
+                // (S(j+2), whose completion tells the other steps, does not exist).
+                if (j + 2 == nkv) mma_commit(smem_u32(&bars.pv_last));
+                return true;
+            };
+            if (ok && nkv > 0) ok = issue_s(0);
+            if (ok && nkv > 1) ok = issue_s(1);
+            for (uint32_t j = 0; j < nkv && ok; ++j) {
+                ok = mbar_wait(smem_u32(&bars.p_full[j & 1u]), (j >> 1) & 1, wait_ns, status,
+                               kStatusTimeout);
                 if (!ok) break;
                 tc_fence_after();
-                bool k_next_ready = false;
-                const uint32_t jn = j + 1;
-                // V(j)'s slot is released as soon as its last P.V MMA is
-                // issued (its commit completes with that MMA), so that the
-                // K tile two steps ahead, which reuses the slot, loads during
-                // the following S MMA rather than after it.
-                const int last_pv = j < tile_n[1] ? 1 : 0;
-                for (int t = 0; t < kNQ && ok; ++t) {
-                    if (j < tile_n[t]) {
-                        ok = mbar_wait(smem_u32(&bars.p_full[t]), j & 1, wait_ns, status, kStatusTimeout);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(t, j);
-                    }
-                    if (t == last_pv) mma_commit(smem_u32(&bars.empty[(2 * j + 1) % kSlots]));
-                    if (jn < tile_n[t]) {
-                        if (!k_next_ready) {
-                            ok = wait_load(2 * jn);
-                            if (!ok) break;
-                            tc_fence_after();
-                            k_next_ready = true;
-                        }
-                        issue_s(t, jn);
-                    }
-                }
-                if (!ok) break;
-                if (k_next_ready) mma_commit(smem_u32(&bars.empty[(2 * jn) % kSlots]));
+                ok = issue_pv(j);
+                if (ok && j + 2 < nkv) ok = issue_s(j + 2);
             }
             if (!ok) record_timeout(status, &bars);
             // Wait until every MMA this thread issued has completed.
@@ -329,25 +342,52 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int t = warp / 4;                 // query tile of this warpgroup
-        const int wq = warp % 4;                // TMEM lane quarter
-        const uint32_t row_in_tile = wq * 32 + lane;
-        const uint32_t tile_row0 = (qt0 + t) * kBM;
+        const uint32_t row_in_tile = warp * 32 + lane;
         const uint32_t row = tile_row0 + row_in_tile;
-        const uint32_t t_s = tmem + t * L::kTileCols + ((uint32_t)(wq * 32) << 16);
-        const uint32_t t_o = t_s + L::kOCol;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_o = lane_base + L::kOCol;
+        const uint32_t sw = row_in_tile & 7u;
         bool ok = true;
+        // ---- prologue: the query row from the staging boxes into TMEM.
+        if (nkv > 0) {
+            ok = mbar_wait(smem_u32(&bars.q_full), 0, wait_ns, status, kStatusTimeout);
+            if (__any_sync(0xffffffffu, !ok)) ok = false;
+            if (ok) {
+                const uint8_t* stage = smem + L::kQStageSlot * kSlotBytes;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    const uint8_t* box_row = stage + c * L::kQBoxBytes + row_in_tile * 128;
+#pragma unroll
+                    for (uint32_t q4 = 0; q4 < 8; ++q4) {
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(box_row + ((q4 ^ sw) * 16));
+                        r[4 * q4] = v4.x;
+                        r[4 * q4 + 1] = v4.y;
+                        r[4 * q4 + 2] = v4.z;
+                        r[4 * q4 + 3] = v4.w;
+                    }
+                    tmem_st32(lane_base + L::kQCol + c * 32, r);
+                }
+                tmem_wait_st();
+            }
+            // The staging reads come before the TMA writes that reuse the
+            // slots, the TMEM stores before the MMAs that read them.
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.q_ready));
+        }
         float m_used = -CUDART_INF_F;  // log2 units
         float l_sum = 0.f;
-        const uint32_t nkv = tile_n[t];
-        for (uint32_t j = 0; j < nkv; ++j) {
-            ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, wait_ns, status, kStatusTimeout);
+        for (uint32_t j = 0; j < nkv && ok; ++j) {
+            const uint32_t buf = j & 1u;
+            ok = mbar_wait(smem_u32(&bars.s_full[buf]), (j >> 1) & 1, wait_ns, status, kStatusTimeout);
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             tc_fence_after();
+            const uint32_t t_s = lane_base + buf * kBK;
             float s[kBK];
             {
                 uint32_t r[kBK];
-                tmem_ld64_sync(t_s, r);
+                tmem_ld128_sync(t_s, r);
 #pragma unroll
                 for (int i = 0; i < kBK; ++i) s[i] = __uint_as_float(r[i]);
             }
@@ -368,7 +408,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             float corr = 1.f;
             bool rescale = false;
             if (m_new > m_used + kRescaleThreshold) {
-                corr = ex2(m_used - m_new);      // 0 on the first tile
+                corr = ex2(m_used - m_new);      // 0 on the first step
                 rescale = (j > 0);
                 m_used = m_new;
             }
@@ -403,6 +443,16 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                  ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             l_sum = fmaf(l_sum, corr, rowsum);
             if (__any_sync(0xffffffffu, rescale)) {
+                // O holds every P.V up to step j-1 once P.V(j-1) has completed:
+                // S(j+1) was issued right after it, and the last step has its
+                // own barrier.  (Waiting on S(j+1) here consumes the same phase
+                // the next step waits for.)
+                ok = j + 1 < nkv ? mbar_wait(smem_u32(&bars.s_full[buf ^ 1u]), ((j + 1) >> 1) & 1,
+                                             wait_ns, status, kStatusTimeout)
+                                 : mbar_wait(smem_u32(&bars.pv_last), 0, wait_ns, status,
+                                             kStatusTimeout);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                tc_fence_after();
                 const float f = rescale ? corr : 1.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -415,20 +465,19 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full[t]));
+            mbar_arrive(smem_u32(&bars.p_full[buf]));
         }
         // ---- epilogue: O (normalised, or this chunk's unnormalised partial)
-        // into the tile's query boxes, then TMA stores of whole lines.
+        // into the ring's first slots, then TMA stores of whole lines.
         const bool split_item = n_chunks > 1;
         if (ok && nkv > 0) {
             ok = mbar_wait(smem_u32(&bars.mma_done), 0, wait_ns, status, kStatusTimeout);
             if (__any_sync(0xffffffffu, !ok)) ok = false;
         }
-        uint8_t* stage = smem + L::kQOff + t * L::kQTileBytes;
+        uint8_t* stage = smem;
         if (ok && nkv > 0) {
             tc_fence_after();
             const float scale_o = split_item ? 1.f : 1.0f / l_sum;
-            const uint32_t sw = row_in_tile & 7u;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
@@ -450,8 +499,8 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             fence_proxy_async_smem();
         }
-        named_barrier(1 + t, 128);
-        if (ok && nkv > 0 && wq == 0 && lane == 0) {
+        named_barrier(1, kSoftmaxThreads);
+        if (ok && nkv > 0 && warp == 0 && lane == 0) {
             const int32_t y0 = (int32_t)tile_row0;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -472,7 +521,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, L::kTmemCols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -545,7 +594,7 @@ cudaError_t launch_tf32(const float* q, const float* k, const float* v, float* o
                         uint32_t kv_stride, float scale, void* workspace, unsigned int* status,
                         uint64_t wait_ns, cudaStream_t stream) {
     using L = Tf32Layout<D>;
-    const PrefillPlan plan = make_plan(m, num_q_heads, D, device_sm_count(), kPerQ);
+    const PrefillPlan plan = make_plan(m, num_q_heads, D, device_sm_count(), kPerQ, 1);
     const Tf32Workspace w = tf32_operands(m, num_kv_heads, D);
     const uint32_t q_cols = num_q_heads * D, kv_cols = num_kv_heads * D;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -616,7 +665,7 @@ cudaError_t launch_tf32(const float* q, const float* k, const float* v, float* o
 
 size_t prefill_tf32_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                     uint32_t head_dim) {
-    const PrefillPlan p = make_plan(m, num_q_heads, head_dim, device_sm_count(), kPerQ);
+    const PrefillPlan p = make_plan(m, num_q_heads, head_dim, device_sm_count(), kPerQ, 1);
     const Tf32Workspace w = tf32_operands(m, num_kv_heads, head_dim);
     return w.kr_bytes + w.vt_bytes + p.part_o_bytes + p.part_ml_bytes;
 }

@@ -325,22 +325,23 @@ def remainder_graphs(bench, stream, append=True):
 TF32_PEAK_RATIO = 1.1 / 2.25
 
 
-def prefill_launches(m, num_q_heads, sms):
+def prefill_launches(m, num_q_heads, sms, tiles_per_item=2):
     """Kernels one tensor-core prefill call launches: the rounding pre-pass
     and the main kernel, plus the combine kernel when the call splits its key
-    walk.  Mirrors the library's split plan: split only when query-tile pairs
-    x heads leave SMs idle, with the smallest chunk whose items fit in one
-    wave."""
+    walk.  Mirrors the library's split plan: a work item is a pair of
+    128-row query tiles (fp16/bf16 kernel) or one tile (TF32 kernel); split
+    only when items x heads leave SMs idle, with the smallest chunk whose
+    items fit in one wave."""
     n_qt = -(-m // 128)
-    n_pairs = -(-m // 256)
+    n_units = -(-m // (128 * tiles_per_item))
 
-    def nk(pr):
-        return min(2 * pr + 2, n_qt)
-    if n_pairs == 0 or n_pairs * num_q_heads >= sms:
+    def nk(u):
+        return min(tiles_per_item * u + tiles_per_item, n_qt)
+    if n_units == 0 or n_units * num_q_heads >= sms:
         return 2
-    nk_last = nk(n_pairs - 1)
+    nk_last = nk(n_units - 1)
     for c in range(2, nk_last):
-        if sum(-(-nk(pr) // c) for pr in range(n_pairs)) * num_q_heads <= sms:
+        if sum(-(-nk(u) // c) for u in range(n_units)) * num_q_heads <= sms:
             return 3
     return 2
 
@@ -364,7 +365,8 @@ class PrefillBench:
         # matrices of 2 bytes per element, 4 in the TF32 mode) and, when the
         # call splits its key walk, the partials that a third kernel merges.
         sms = torch.cuda.get_device_properties(device).multi_processor_count
-        self.launches_per_call = prefill_launches(shape.m, shape.num_q_heads, sms)
+        self.launches_per_call = prefill_launches(
+            shape.m, shape.num_q_heads, sms, 1 if self.prec == attn.ATTN_PREC_TF32 else 2)
 
     def call(self, i, stream):
         c, a, r = self.c, self.attn, i % self.R
