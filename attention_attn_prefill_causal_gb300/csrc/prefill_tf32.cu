@@ -37,8 +37,13 @@
 // then per step j: P(j).V, then S(j+2) into the buffer P(j) occupied (MMAs
 // execute in issue order, so S(j+2) overwrites P(j) after P(j).V has read
 // it).  A slot is released by a commit right after the MMAs that read it.
-// Warp roles (192 threads): warps 0-3 softmax (thread = TMEM lane = query
-// row), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer.
+// Warp roles (224 threads): warps 0-3 softmax (thread = TMEM lane = query
+// row), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer, warp 6
+// gate.  An mbarrier wait on the issuing thread stalls the tensor pipe even
+// when the phase has already completed (about 26 ns each, measured), so the
+// MMA thread waits once per step: on go(j), which the 128 softmax threads
+// complete with P(j) and the gate thread with the slots of V(j) and K(j+2)
+// (the gate waits for each slot's load in turn).
 // The softmax rescales O only when the running max grows by more than 8
 // (log2 units); it then first waits for the previous P.V (O stable).
 // Epilogue: O (normalised, or a chunk's unnormalised partial) into the ring's
@@ -72,9 +77,10 @@ constexpr uint32_t kPerQ = kBM / kBK;  // key tiles per 128-key block (1)
 constexpr int kSlots = 7;              // operand ring slots
 constexpr uint32_t kSlotBytes = 32 * 1024;
 constexpr int kSoftmaxThreads = 128;   // warps 0-3
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
+constexpr int kGateWarp = 6;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // the bits of an fp32 a TF32 operand keeps
 
@@ -107,7 +113,7 @@ struct __align__(8) Tf32Barriers {
     uint64_t full[kSlots];
     uint64_t empty[kSlots];
     uint64_t s_full[2];     // S(j) in buffer j % 2 computed
-    uint64_t p_full[2];     // P(j) in buffer j % 2 written
+    uint64_t go[2];         // step j % 2: P(j) written and the slots of V(j), K(j+2) loaded
     uint64_t pv_last;       // P.V of the second-to-last step completed (one phase)
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -172,7 +178,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&bars.s_full[b]), 1);
-            mbar_init(smem_u32(&bars.p_full[b]), kSoftmaxThreads);
+            mbar_init(smem_u32(&bars.go[b]), kSoftmaxThreads + 1);
         }
         mbar_init(smem_u32(&bars.pv_last), 1);
         mbar_init(smem_u32(&bars.mma_done), 1);
@@ -278,13 +284,15 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // 128-byte swizzled row, in box ks / 4 of its piece.
             const uint64_t dr0 = smem_desc(sR, 16, 1024, 2);
             uint32_t load = 0;  // next load the MMAs consume
-            auto take = [&](uint64_t& desc, uint32_t& slot) {
+            // S(0) and S(1) wait for their slots here; every later slot is
+            // covered by the go barrier of its step.
+            auto take = [&](uint64_t& desc, uint32_t& slot, bool wait) {
                 slot = load % kSlots;
-                const bool got = mbar_wait(smem_u32(&bars.full[slot]), (load / kSlots) & 1, wait_ns,
-                                           status, kStatusTimeout);
+                const bool got = !wait || mbar_wait(smem_u32(&bars.full[slot]), (load / kSlots) & 1,
+                                                    wait_ns, status, kStatusTimeout);
                 desc = dr0 + (uint64_t)(slot * (kSlotBytes / 16));
                 ++load;
-                if (got) tc_fence_after();
+                if (got && wait) tc_fence_after();
                 return got;
             };
             auto issue_s = [&](uint32_t j) {
@@ -292,7 +300,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int p = 0; p < L::kPieces; ++p) {
                     uint64_t b0;
                     uint32_t slot;
-                    if (!take(b0, slot)) return false;
+                    if (!take(b0, slot, j < 2)) return false;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {
                         const int k = p * 8 + ks;  // 8 of the D columns per MMA
@@ -310,7 +318,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int p = 0; p < L::kPieces; ++p) {
                     uint64_t b0;
                     uint32_t slot;
-                    if (!take(b0, slot)) return false;
+                    take(b0, slot, false);
 #pragma unroll
                     for (int ks = 0; ks < L::kVStepsPerPiece; ++ks) {
                         const int k = p * L::kVStepsPerPiece + ks;  // 8 keys per MMA
@@ -328,7 +336,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (ok && nkv > 0) ok = issue_s(0);
             if (ok && nkv > 1) ok = issue_s(1);
             for (uint32_t j = 0; j < nkv && ok; ++j) {
-                ok = mbar_wait(smem_u32(&bars.p_full[j & 1u]), (j >> 1) & 1, wait_ns, status,
+                ok = mbar_wait(smem_u32(&bars.go[j & 1u]), (j >> 1) & 1, wait_ns, status,
                                kStatusTimeout);
                 if (!ok) break;
                 tc_fence_after();
@@ -339,6 +347,28 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // Wait until every MMA this thread issued has completed.
             mma_commit(smem_u32(&bars.mma_done));
             mbar_wait(smem_u32(&bars.mma_done), 0, kDrainWaitNs);
+        }
+    } else if (warp == kGateWarp) {
+        // ------------------------------------------------------------ gate
+        // Step j's MMAs read the loads [load, load + pieces of V(j) and
+        // K(j+2)); S(0) and S(1) took the first ones.  go(j) reuses the
+        // barrier of step j - 2, whose phase must complete first (its P
+        // arrivals precede this step's, so none can land in the old phase).
+        if (lane == 0) {
+            uint32_t load = (uint32_t)L::kPieces * min(nkv, 2u);
+            bool ok = true;
+            for (uint32_t j = 0; j < nkv && ok; ++j) {
+                if (j >= 2)
+                    ok = mbar_wait(smem_u32(&bars.go[j & 1u]), ((j - 2) >> 1) & 1, wait_ns, status,
+                                   kStatusTimeout);
+                const uint32_t n = (uint32_t)L::kPieces * (j + 2 < nkv ? 2u : 1u);
+                for (uint32_t i = 0; i < n && ok; ++i, ++load)
+                    ok = mbar_wait(smem_u32(&bars.full[load % kSlots]), (load / kSlots) & 1, wait_ns,
+                                   status, kStatusTimeout);
+                if (!ok) break;
+                mbar_arrive(smem_u32(&bars.go[j & 1u]));
+            }
+            if (!ok) record_timeout(status, &bars);
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -465,7 +495,7 @@ prefill_tf32_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full[buf]));
+            mbar_arrive(smem_u32(&bars.go[buf]));
         }
         // ---- epilogue: O (normalised, or this chunk's unnormalised partial)
         // into the ring's first slots, then TMA stores of whole lines.
