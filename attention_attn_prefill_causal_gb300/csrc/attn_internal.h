@@ -111,6 +111,17 @@ cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, fl
                               float scale, bool bf16, void* workspace, unsigned int* status,
                               uint64_t wait_limit_ns, cudaStream_t stream);
 
+// The 16-bit kernel over query-tile pairs (prefill_tc_pair.cu), which
+// launch_prefill_tc takes for grids of at least two waves of pairs.
+bool prefill_use_pairs(uint32_t m, uint32_t num_q_heads, int sm_count);
+size_t prefill_pair_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                    uint32_t head_dim);
+cudaError_t launch_prefill_pair(const float* q, const float* k, const float* v, float* o,
+                                uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
+                                float scale, bool bf16, void* workspace, unsigned int* status,
+                                uint64_t wait_limit_ns, cudaStream_t stream);
+
 size_t prefill_tf32_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                     uint32_t head_dim);
 

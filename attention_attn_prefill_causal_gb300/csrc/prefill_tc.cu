@@ -1,57 +1,67 @@
 // prefill_tc.cu -- causal grouped-query prefill on the Blackwell tensor cores
-// (tcgen05 MMAs with TMEM accumulators, TMA-staged tiles).
+// (tcgen05 MMAs with TMEM accumulators, TMA-staged tiles), one kernel for the
+// three operand types: fp16, bf16 (kind::f16) and TF32 (kind::tf32).
 //
 // Operation ("aprender-gpu 0.32.0 -- prefill_fused.rs", module doc,
 // Algorithm 1-3): for query head h and KV head g = h / heads_per_kv, row i
-// of O is sum_{j<=i} softmax_j(scale * Q[i].K[j]) V[j], computed with an
-// online softmax.  The page does this with one warp per head on CUDA cores;
-// here the two contractions (S = Q K^T and O += P V) run on the tensor core.
+// of O is sum_{j<=i} softmax_j(scale * Q[i].K[j]) V[j], with an online
+// softmax.  The page does this with one warp per head on CUDA cores; here
+// the two contractions (S = Q K^T and O += P V) run on the tensor core, and
+// the softmax statistics (row max, row sum) and the output stay fp32.
 //
-// Precision: Q, K, V (fp32, packed strides) are rounded to fp16 with
-// round-to-nearest (10-bit mantissa, the same as TF32): K and V by a pre-pass
-// into a workspace, Q inside this kernel (each CTA stages its two fp32 query
-// tiles with TMA and the softmax warps round them once).  The softmax writes
-// P as fp16, and every MMA accumulates in fp32.  Softmax statistics (row max,
-// row sum) and the output stay fp32.
+// Precision.  fp16 / bf16: Q, K, V are rounded to nearest (K and V by a
+// pre-pass into a workspace, Q by the softmax warps as they move it into
+// TMEM); P is rounded to nearest as the softmax packs it; fp16 inputs must
+// stay below 65504 (kStatusRange otherwise, after the fact).  TF32: a
+// kind::tf32 MMA uses the top 19 bits of each fp32 operand (the low 13
+// mantissa bits are dropped).  Q goes to the tensor core as the caller
+// stored it.  K and V are rounded to nearest TF32 by the pre-pass: an operand
+// dropped toward zero would bias the output (O = V[0] exactly for row 0),
+// which rounding to nearest halves and unbiases.  P is truncated to TF32 by
+// the softmax itself and the row sum is taken over the truncated weights, so
+// the weights the MMA applies are normalised exactly (a row sum over the
+// untruncated weights would scale every output down by up to 2^-10 where the
+// running max lags the row's largest score).
 //
-// CTA work unit: two consecutive 128-row query tiles (A = rows q0..q0+127,
-// B = q0+128..q0+255) of one head; keys are walked in 128-row tiles up to the
-// diagonal.  Warp roles (320 threads):
-//   warps 0-3  softmax for tile A  (thread r owns TMEM lane r = query row r)
-//   warps 4-7  softmax for tile B
-//   warp  8    TMA producer: both fp32 Q tiles once (staged in the K and
-//              V rings, which the softmax warps then free by rounding them
-//              into the fp16 Q tiles), then K and V tiles into a
-//              two-stage ring
-//   warp  9    TMEM allocator and MMA issuer (one thread)
-// TMEM (512 columns): per tile, S/P in 128 columns (P is written as packed
-// fp16 pairs over the first 64 columns of S) and O in head_dim columns.
-// The MMA thread ping-pongs: while softmax A works on S_A(j), the tensor core
-// runs PV_B(j-1) and S_B(j); while softmax B works, it runs PV_A(j) and
-// S_A(j+1).  tcgen05 MMAs issued by one thread execute in order, so S_t(j+1)
-// may overwrite the TMEM that held P_t(j) right after PV_t(j) is issued, and
-// the commit that signals S_t(j+1) also covers PV_t(j): once softmax t sees
-// S_t(j+1) its O accumulator is stable and can be rescaled.
-// The MMA thread builds each operand tile's descriptor once and reaches the
-// operand of every K step with one 64-bit add: work between consecutive MMAs
-// on the issuing thread directly lowers the rate the tensor pipe is fed at.
-// Rescaling is conditional: the running max used for the exponentials only
-// moves when the row max grows by more than 8 (log2 units); the final O / l
-// is exact either way, and P stays below 2^8.
-// Epilogue: after the CTA's last MMA the K/V ring is free; each softmax
-// thread writes its row of O into 128-byte swizzled staging boxes there, and
-// one thread per tile stores them with TMA tensor stores, so O leaves in
-// whole 128-byte lines rather than one 16-byte piece per row and instruction.
-// Small grids (query-tile pairs x heads below the SM count) split each
-// pair's key walk into chunks of C tiles, one work item per chunk; chunks
-// write unnormalised partials and a combine kernel merges them.
-// Launch chain: the rounding pre-pass waits for the kernel before the call
-// and then lets this kernel launch; this kernel stages the caller's fp32 Q at
-// once and waits for the pre-pass only before its first K tile; the combine
-// waits for this kernel (all programmatic dependent launches).
+// Layout.  16-bit: the pre-pass writes K and V rounded, [m, kv_heads*D];
+// S reads K K-major and P.V reads V MN-major (keys are the K dimension, D is
+// contiguous).  TF32 MMAs take only K-major operands, so the pre-pass writes
+// V rounded and transposed per KV head, [kv_heads*D, m4] fp32 (keys
+// contiguous, m4 = m rounded up to 4).
+//
+// CTA work unit: one 128-row query tile of one head; keys are walked in
+// 128-key steps up to the diagonal.  With S double-buffered in TMEM the
+// tensor core computes S(j+1) and P(j-1).V while the softmax works on S(j),
+// so a single tile keeps it busy.  TMEM (512 columns): S/P buffers 0 and 1
+// (128 columns each; 16-bit P is packed in pairs over the first 64), O (D
+// columns) and the query tile (D columns in TF32, D/2 packed 16-bit pairs;
+// the S MMA takes A from TMEM, so shared memory feeds it only K).  Shared
+// memory holds only a ring of seven 32 KB slots: a K or V tile is one piece
+// (16-bit) or D/64 pieces (TF32) of at most 32 KB, loaded in the order the
+// MMAs consume them: K(0), K(1), V(0), K(2), V(1), K(3), ...  The MMA thread
+// issues S(0), S(1), then per step j: P(j).V, then S(j+2) into the buffer
+// P(j) occupied (MMAs execute in issue order, so S(j+2) overwrites P(j)
+// after P(j).V has read it).  A slot is released by a commit right after the
+// MMAs that read it.
+// Warp roles (224 threads): warps 0-3 softmax (thread = TMEM lane = query
+// row), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer, warp 6
+// gate.  An mbarrier wait on the issuing thread stalls the tensor pipe even
+// when the phase has already completed (about 26 ns each, measured), so the
+// MMA thread waits once per step: on go(j), which the 128 softmax threads
+// complete with P(j) and the gate thread with the slots of V(j) and K(j+2)
+// (the gate waits for each slot's load in turn).
+// The softmax rescales O only when the running max grows by more than 8
+// (log2 units); it then first waits for the previous P.V (O stable).
+// Epilogue: O (normalised, or a chunk's unnormalised partial) into the ring's
+// first slots, then TMA stores of whole 128-byte lines.  Small grids split
+// each tile's key walk into chunks merged by the combine kernel.
+// Launch chain (programmatic dependent launches): the pre-pass waits for the
+// kernel before the call, then lets this kernel launch; this kernel stages
+// the caller's Q at once and waits for the pre-pass before its first K/V
+// load; the combine waits for this kernel.
 // Every mbarrier wait is bounded; on a timeout a thread records
-// kStatusTimeout in the device status word, abandons its loop, and the CTA
-// still drains its copies, waits for its MMAs and frees TMEM before exiting.
+// kStatusTimeout, abandons its loop, and the CTA still drains its copies,
+// waits for its MMAs and frees TMEM before exiting.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -59,8 +69,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <algorithm>
 #include <cstdint>
-#include <mutex>
 
 #include "attn_internal.h"
 #include "prefill_tc_common.cuh"
@@ -71,68 +81,79 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBN = 128;            // keys per KV tile
-constexpr int kStages = 2;          // K/V ring depth
-constexpr int kThreads = 320;
-constexpr int kSoftmaxThreads = 256;  // warps 0-7
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr uint32_t kTmemCols = 512;
+enum class Op : int { FP16 = 0, BF16 = 1, TF32 = 2 };
 
-template <int D>
+constexpr int kBK = 128;               // keys per step
+constexpr uint32_t kPerQ = kBM / kBK;  // key tiles per 128-key block (1)
+constexpr int kSlots = 7;              // operand ring slots
+constexpr uint32_t kSlotBytes = 32 * 1024;
+constexpr int kSoftmaxThreads = 128;   // warps 0-3
+constexpr int kThreads = 224;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kGateWarp = 6;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTf32Mask = 0xFFFFE000u;  // the bits of an fp32 a TF32 operand keeps
+constexpr uint32_t kBoxBytes = kBK * 128;    // 128 rows x 128 bytes, 128-byte swizzled
+
+template <int D, Op OP>
 struct TcLayout {
-    static constexpr uint32_t kBoxes = D / 64;                  // 64 fp16 = 128 B per box row
-    static constexpr uint32_t kQTileBytes = kBM * D * 2;
-    static constexpr uint32_t kKTileBytes = kBN * D * 2;
-    static constexpr uint32_t kQOff = 0;
-    static constexpr uint32_t kKOff = kQOff + kNQ * kQTileBytes;
-    static constexpr uint32_t kVOff = kKOff + kStages * kKTileBytes;
-    static constexpr uint32_t kBytes = kVOff + kStages * kKTileBytes;
-    static constexpr uint32_t kSmemAlloc = kBytes + 1024;        // room to align to 1 KB
-    // Epilogue: once every MMA has completed, the K/V ring stages the fp32
-    // output tiles for the TMA stores, as D/32 boxes of 128 rows x 128 bytes
-    // (32 floats) in the 128-byte swizzled layout.
-    static constexpr uint32_t kOBoxBytes = kBM * 128;
-    static constexpr uint32_t kOTileBytes = kBM * D * 4;
-    static constexpr uint32_t kStageOff = kKOff;
-    static_assert(kStageOff + kNQ * kOTileBytes <= kBytes, "output staging exceeds the K/V ring");
-    // Prologue: the two fp32 query tiles (D/32 boxes of 128 rows x 32 floats,
-    // 128-byte swizzled) are staged at once, tile 0 in the K ring and tile 1
-    // in the V ring, before K and V are first loaded.
-    static constexpr uint32_t kQ32Bytes = kBM * D * 4;
-    __host__ __device__ static constexpr uint32_t q32_off(int t) { return t == 0 ? kKOff : kVOff; }
-    static_assert(kQ32Bytes <= kStages * kKTileBytes, "fp32 query tile exceeds a K/V ring");
+    static constexpr bool k16 = OP != Op::TF32;
+    static constexpr uint32_t kElem = k16 ? 2 : 4;
+    static constexpr uint32_t kBoxElems = 128 / kElem;               // elements per box row
+    static constexpr uint32_t kTileBytes = kBK * D * kElem;          // one K or V tile
+    static constexpr int kPieces = kTileBytes > kSlotBytes ? (int)(kTileBytes / kSlotBytes) : 1;
+    static constexpr uint32_t kPieceBytes = kTileBytes / kPieces;
+    static constexpr int kKBoxesPerPiece = (int)(D * kElem / 128) / kPieces;  // D-column boxes
+    // 16-bit V: boxes of 64 D-columns x 128 keys; TF32 V^T: boxes of 32 keys x D rows.
+    static constexpr uint32_t kVBoxBytes = k16 ? kBoxBytes : D * 128;
+    static constexpr int kVBoxesPerPiece = k16 ? kKBoxesPerPiece : 4 / kPieces;
+    static constexpr int kSSteps = (int)(D * kElem / 32) / kPieces;  // S MMAs per K piece (32 B of K each)
+    static constexpr int kVSteps = k16 ? kBK / 16 : kBK / 8 / kPieces;  // P.V MMAs per V piece
+    static constexpr uint32_t kQ32Bytes = kBM * D * 4;               // fp32 query or output tile
+    static constexpr int kQSlots = (int)(kQ32Bytes / kSlotBytes);
+    static constexpr int kQStageSlot = kSlots - kQSlots;
+    static constexpr uint32_t kBytes = kSlots * kSlotBytes;
+    static constexpr uint32_t kSmemAlloc = kBytes + 1024;            // room to align to 1 KB
+    static constexpr uint32_t kOCol = 2 * kBK;                       // TMEM: S0 | S1 | O | Q
+    static constexpr uint32_t kQCol = kOCol + D;
+    static constexpr uint32_t kQCols = k16 ? D / 2 : D;
+    static_assert(kQCol + kQCols <= kTmemCols, "TMEM layout");
+    static_assert(kPieceBytes <= kSlotBytes && kPieces * kPieceBytes == kTileBytes, "pieces");
+    static_assert(kKBoxesPerPiece * kBoxBytes == kPieceBytes, "K piece");
+    static_assert(kVBoxesPerPiece * kVBoxBytes == kPieceBytes, "V piece");
+    static_assert(kQSlots * kSlotBytes == kQ32Bytes, "query staging");
+    static_assert(kSmemAlloc <= 227 * 1024, "shared memory");
 };
 
 struct __align__(8) TcBarriers {
-    uint64_t q_staged[kNQ];   // fp32 Q tile t landed in the staging area
-    uint64_t q_ready[kNQ];    // fp16 Q tile t written (every softmax thread arrives)
-    uint64_t k_full[kStages];
-    uint64_t k_empty[kStages];
-    uint64_t v_full[kStages];
-    uint64_t v_empty[kStages];
-    uint64_t s_full[kNQ];
-    uint64_t p_full[kNQ];
+    uint64_t q_full;        // the fp32 query tile landed in the staging slots
+    uint64_t q_ready;       // the query tile is in TMEM (every softmax thread arrives)
+    uint64_t full[kSlots];
+    uint64_t empty[kSlots];
+    uint64_t s_full[2];     // S(j) in buffer j % 2 computed
+    uint64_t go[2];         // step j % 2: P(j) written and the slots of V(j), K(j+2) loaded
+    uint64_t pv_last;       // P.V of the second-to-last step completed (one phase)
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t abort;
 };
-
-__device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16) {
-    if (bf16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
 
 __device__ __forceinline__ void record_timeout(unsigned int* status, TcBarriers* bars) {
     atomicOr(status, kStatusTimeout);
     atomicExch(&bars->abort, 1u);
 }
 
-template <int D, bool BF16>
+template <Op OP>
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    if constexpr (OP == Op::TF32)
+        mma_tf32_ts(d, a, b, idesc, accumulate);
+    else
+        mma_f16_ts(d, a, b, idesc, accumulate);
+}
+
+template <int D, Op OP>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -140,28 +161,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   uint32_t num_q_heads, uint32_t heads_per_kv,
                   float scale_log2, unsigned int* status, uint64_t wait_ns,
                   const SplitArgs split) {
-    using L = TcLayout<D>;
+    using L = TcLayout<D, OP>;
+    constexpr bool k16 = L::k16;
+    constexpr bool kBf16 = OP == Op::BF16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     __shared__ TcBarriers bars;
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t n_pairs = (m + kNQ * kBM - 1) / (kNQ * kBM);
+    const uint32_t n_qt = (m + kBM - 1) / kBM;
     const uint32_t h = blockIdx.x % num_q_heads;
     const uint32_t kvh = h / heads_per_kv;
-    // Work item: (query-tile pair, KV chunk).  Pairs are walked heaviest
-    // first; without a split every pair is one chunk covering all its keys.
-    uint32_t pair = 0, chunk = 0, n_chunks = 1;
+    // Work item: (query tile, key chunk), heaviest tiles first.
+    uint32_t qt = 0, chunk = 0, n_chunks = 1;
     if (split.kv_chunk == kNoSplit) {
-        pair = n_pairs - 1 - blockIdx.x / num_q_heads;
+        qt = n_qt - 1 - blockIdx.x / num_q_heads;
     } else {
         uint32_t idx = blockIdx.x / num_q_heads;
-        for (int p = (int)n_pairs - 1; p >= 0; --p) {
-            const uint32_t nk = max(kv_tiles_for(p * kNQ, m, 1), kv_tiles_for(p * kNQ + 1, m, 1));
-            const uint32_t nc = (nk + split.kv_chunk - 1) / split.kv_chunk;
+        for (int t = (int)n_qt - 1; t >= 0; --t) {
+            const uint32_t nc = (kv_tiles_for(t, m, kPerQ) + split.kv_chunk - 1) / split.kv_chunk;
             if (idx < nc) {
-                pair = (uint32_t)p;
+                qt = (uint32_t)t;
                 chunk = idx;
                 n_chunks = nc;
                 break;
@@ -169,41 +190,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             idx -= nc;
         }
     }
-    const uint32_t qt0 = pair * kNQ;                                // first query tile index
-    uint32_t n_kv[kNQ];
-#pragma unroll
-    for (int t = 0; t < kNQ; ++t) n_kv[t] = kv_tiles_for(qt0 + t, m, 1);
-    uint32_t n_kv_pair = 0;
-#pragma unroll
-    for (int t = 0; t < kNQ; ++t) n_kv_pair = max(n_kv_pair, n_kv[t]);
-    // This item's KV tiles are [j0, j0 + n_it); tile t takes the first tile_n[t]
-    // of them (its causal extent may end inside the chunk).
+    const uint32_t n_kv_tile = kv_tiles_for(qt, m, kPerQ);
+    // This item's key steps are [j0, j0 + nkv).
     const uint32_t j0 = split.kv_chunk == kNoSplit ? 0u : chunk * split.kv_chunk;
-    const uint32_t n_kv_all =
-        split.kv_chunk == kNoSplit ? n_kv_pair : min(n_kv_pair, j0 + split.kv_chunk) - j0;
-    uint32_t tile_n[kNQ];
-#pragma unroll
-    for (int t = 0; t < kNQ; ++t) tile_n[t] = n_kv[t] > j0 ? min(n_kv[t] - j0, n_kv_all) : 0;
+    const uint32_t nkv =
+        split.kv_chunk == kNoSplit ? n_kv_tile : min(n_kv_tile, j0 + split.kv_chunk) - j0;
+    const uint32_t tile_row0 = qt * kBM;
 
-    const uint32_t sQ = smem_u32(smem + L::kQOff);
-    const uint32_t sK = smem_u32(smem + L::kKOff);
-    const uint32_t sV = smem_u32(smem + L::kVOff);
+    const uint32_t sR = smem_u32(smem);
 
     if (threadIdx.x == 0) {
-        for (int t = 0; t < kNQ; ++t) {
-            mbar_init(smem_u32(&bars.q_staged[t]), 1);
-            mbar_init(smem_u32(&bars.q_ready[t]), kSoftmaxThreads);
+        mbar_init(smem_u32(&bars.q_full), 1);
+        mbar_init(smem_u32(&bars.q_ready), kSoftmaxThreads);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(smem_u32(&bars.full[s]), 1);
+            mbar_init(smem_u32(&bars.empty[s]), 1);
         }
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&bars.k_full[s]), 1);
-            mbar_init(smem_u32(&bars.k_empty[s]), 1);
-            mbar_init(smem_u32(&bars.v_full[s]), 1);
-            mbar_init(smem_u32(&bars.v_empty[s]), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&bars.s_full[b]), 1);
+            mbar_init(smem_u32(&bars.go[b]), kSoftmaxThreads + 1);
         }
-        for (int t = 0; t < kNQ; ++t) {
-            mbar_init(smem_u32(&bars.s_full[t]), 1);
-            mbar_init(smem_u32(&bars.p_full[t]), kBM);
-        }
+        mbar_init(smem_u32(&bars.pv_last), 1);
         mbar_init(smem_u32(&bars.mma_done), 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -219,254 +226,278 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
+    // Loads of the item, in the order the MMAs consume them: K(0), K(1),
+    // then V(i) and K(i + 2) alternately.  Unit u is one tile; load n is
+    // piece n % kPieces of unit n / kPieces.
+    const uint32_t n_units = nkv > 0 ? 2 * nkv : 0;
+    auto unit_of = [&](uint32_t u, bool& is_k, uint32_t& step) {
+        if (u < 2 && u < nkv) { is_k = true; step = u; return; }
+        // after K(0) and K(1): V(i) at 2 + 2i (with K(i+2) at 3 + 2i while i + 2 < nkv);
+        // once the keys run out, the remaining units are V tiles only
+        const uint32_t first_v = nkv < 2 ? nkv : 2u;
+        const uint32_t r = u - first_v;
+        const uint32_t paired = nkv > 2 ? nkv - 2 : 0u;  // V(i) followed by K(i+2) for i < paired
+        if (r < 2 * paired) {
+            is_k = (r & 1u) != 0;
+            step = is_k ? r / 2 + 2 : r / 2;
+        } else {
+            is_k = false;
+            step = paired + (r - 2 * paired);
+        }
+    };
+
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            auto load_q32 = [&](int t) {
-                const uint32_t dst = smem_u32(smem + L::q32_off(t));
-                mbar_arrive_expect_tx(smem_u32(&bars.q_staged[t]), L::kQ32Bytes);
+            {
+                const uint32_t bar = smem_u32(&bars.q_full);
+                mbar_arrive_expect_tx(bar, L::kQ32Bytes);
                 for (uint32_t b = 0; b < D / 32; ++b)
-                    tma_load_2d(dst + b * L::kOBoxBytes, &tm_q, smem_u32(&bars.q_staged[t]),
-                                (int32_t)(h * D + b * 32), (int32_t)((qt0 + t) * kBM));
-            };
-            auto load_k = [&](uint32_t j) {
-                const uint32_t st = j % kStages;
-                mbar_arrive_expect_tx(smem_u32(&bars.k_full[st]), L::kKTileBytes);
-                for (uint32_t b = 0; b < L::kBoxes; ++b)
-                    tma_load_2d(sK + st * L::kKTileBytes + b * (kBN * 128), &tm_k,
-                                smem_u32(&bars.k_full[st]), (int32_t)(kvh * D + b * 64),
-                                (int32_t)((j0 + j) * kBN));
-            };
-            auto load_v = [&](uint32_t j) {
-                const uint32_t st = j % kStages;
-                mbar_arrive_expect_tx(smem_u32(&bars.v_full[st]), L::kKTileBytes);
-                for (uint32_t b = 0; b < L::kBoxes; ++b)
-                    tma_load_2d(sV + st * L::kKTileBytes + b * (kBN * 128), &tm_v,
-                                smem_u32(&bars.v_full[st]), (int32_t)(kvh * D + b * 64),
-                                (int32_t)((j0 + j) * kBN));
-            };
-            // Both query tiles at once; the first K tile as soon as tile 0
-            // (staged in the K ring) is converted, V after tile 1.
-            uint32_t q_issued = 0, k_issued = 0, v_issued = 0;
-            load_q32(0);
-            load_q32(1);
-            q_issued = 2;
-            // The kernel is a programmatic dependent of the rounding pre-pass.
-            // Q is the caller's (its writer finished before the pre-pass
-            // began), so it is staged at once; the fp16 K and V the pre-pass
-            // writes are read only once that grid has completed.
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            bool ok = mbar_wait(smem_u32(&bars.q_ready[0]), 0, wait_ns, status, kStatusTimeout);
-            if (ok && n_kv_all > 0) {
-                load_k(0);
-                k_issued = 1;
+                    tma_load_2d(sR + L::kQStageSlot * kSlotBytes + b * kBoxBytes, &tm_q, bar,
+                                (int32_t)(h * D + b * 32), (int32_t)tile_row0);
             }
-            if (ok) ok = mbar_wait(smem_u32(&bars.q_ready[1]), 0, wait_ns, status, kStatusTimeout);
-            for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
-                const uint32_t st = j % kStages;
-                const uint32_t use = j / kStages;
-                if (j >= k_issued) {
-                    if (use > 0) ok = mbar_wait(smem_u32(&bars.k_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
-                    if (!ok) break;
-                    load_k(j);
-                    k_issued = j + 1;
+            // K and V come from the pre-pass: read them only once its grid
+            // (and with it every kernel before the call) has completed.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            const uint32_t n_loads = n_units * L::kPieces;
+            uint32_t issued = 0;
+            bool ok = true;
+            for (uint32_t n = 0; n < n_loads; ++n) {
+                const uint32_t slot = n % kSlots, use = n / kSlots;
+                if (use > 0) {
+                    ok = mbar_wait(smem_u32(&bars.empty[slot]), (use - 1) & 1, wait_ns, status,
+                                   kStatusTimeout);
+                } else if (slot >= (uint32_t)L::kQStageSlot) {
+                    // the query staging slots are free once the tile is in TMEM
+                    ok = mbar_wait(smem_u32(&bars.q_ready), 0, wait_ns, status, kStatusTimeout);
                 }
-                if (use > 0) ok = mbar_wait(smem_u32(&bars.v_empty[st]), (use - 1) & 1, wait_ns, status, kStatusTimeout);
                 if (!ok) break;
-                load_v(j);
-                v_issued = j + 1;
+                bool is_k;
+                uint32_t step;
+                unit_of(n / L::kPieces, is_k, step);
+                const uint32_t piece = n % L::kPieces;
+                const uint32_t bar = smem_u32(&bars.full[slot]);
+                const uint32_t dst = sR + slot * kSlotBytes;
+                const uint32_t key0 = (j0 + step) * kBK;
+                mbar_arrive_expect_tx(bar, L::kPieceBytes);
+                if (is_k) {
+                    for (int b = 0; b < L::kKBoxesPerPiece; ++b)
+                        tma_load_2d(dst + b * kBoxBytes, &tm_k, bar,
+                                    (int32_t)(kvh * D + (piece * L::kKBoxesPerPiece + b) * L::kBoxElems),
+                                    (int32_t)key0);
+                } else if constexpr (k16) {
+                    for (int b = 0; b < L::kVBoxesPerPiece; ++b)
+                        tma_load_2d(dst + b * kBoxBytes, &tm_v, bar,
+                                    (int32_t)(kvh * D + b * L::kBoxElems), (int32_t)key0);
+                } else {
+                    for (int b = 0; b < L::kVBoxesPerPiece; ++b)
+                        tma_load_2d(dst + b * L::kVBoxBytes, &tm_v, bar,
+                                    (int32_t)(key0 + (piece * L::kVBoxesPerPiece + b) * 32),
+                                    (int32_t)(kvh * D));
+                }
+                issued = n + 1;
             }
             if (!ok) record_timeout(status, &bars);
             // Drain: every copy this CTA issued must land before it exits.
-            for (uint32_t t = 0; t < q_issued; ++t)
-                mbar_wait(smem_u32(&bars.q_staged[t]), 0, kDrainWaitNs);
-            for (uint32_t j = (k_issued > kStages ? k_issued - kStages : 0); j < k_issued; ++j)
-                mbar_wait(smem_u32(&bars.k_full[j % kStages]), (j / kStages) & 1, kDrainWaitNs);
-            for (uint32_t j = (v_issued > kStages ? v_issued - kStages : 0); j < v_issued; ++j)
-                mbar_wait(smem_u32(&bars.v_full[j % kStages]), (j / kStages) & 1, kDrainWaitNs);
+            mbar_wait(smem_u32(&bars.q_full), 0, kDrainWaitNs);
+            for (uint32_t n = (issued > kSlots ? issued - kSlots : 0); n < issued; ++n)
+                mbar_wait(smem_u32(&bars.full[n % kSlots]), (n / kSlots) & 1, kDrainWaitNs);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16(BF16 ? 1u : 0u, 0, 0, kBN, kBM);
-            const uint32_t idesc_pv = idesc_f16(BF16 ? 1u : 0u, 0, 1, D, kBM);
-            bool ok = true;
-            for (int t = 0; t < kNQ && ok; ++t)
-                ok = mbar_wait(smem_u32(&bars.q_ready[t]), 0, wait_ns, status, kStatusTimeout);
-            // Descriptor bases, built once.  A descriptor keeps the start
-            // address as (address >> 4) in its low 14 bits, so an operand at
-            // byte offset off inside a tile is the tile's descriptor plus
-            // off >> 4 (shared-memory offsets stay below 256 KB: no carry).
-            // Each MMA below is then one 64-bit add away from issue: building
-            // descriptors between MMAs measured at less than half the MMA
-            // rate a single issuing thread reaches without it.
-            const uint64_t dq0 = smem_desc(sQ, 16, 1024, 2);
-            const uint64_t dq1 = smem_desc(sQ + L::kQTileBytes, 16, 1024, 2);
-            const uint64_t dk0 = smem_desc(sK, 16, 1024, 2);
-            const uint64_t dk1 = smem_desc(sK + L::kKTileBytes, 16, 1024, 2);
-            const uint64_t dv0 = smem_desc(sV, kBN * 128, 1024, 2);
-            const uint64_t dv1 = smem_desc(sV + L::kKTileBytes, kBN * 128, 1024, 2);
-            static_assert(kNQ == 2 && kStages == 2, "descriptor bases assume two tiles and two stages");
-            auto issue_s = [&](int t, uint32_t j) {
-                const uint64_t a0 = t == 0 ? dq0 : dq1;
-                const uint64_t b0 = (j % kStages) == 0 ? dk0 : dk1;
-                const uint32_t d = tmem + t * 256;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t offa = (uint64_t)((ks / 4) * (kBM * 128 / 16) + (ks % 4) * 2);
-                    const uint64_t offb = (uint64_t)((ks / 4) * (kBN * 128 / 16) + (ks % 4) * 2);
-                    mma_f16_ss(d, a0 + offa, b0 + offb, idesc_s, ks > 0 ? 1u : 0u);
-                }
-                mma_commit(smem_u32(&bars.s_full[t]));
+            constexpr uint32_t kAb = kBf16 ? 1u : 0u;
+            constexpr uint32_t idesc_s = k16 ? idesc_f16(kAb, 0, 0, kBK, kBM) : idesc_tf32(kBK, kBM);
+            constexpr uint32_t idesc_pv = k16 ? idesc_f16(kAb, 0, 1, D, kBM) : idesc_tf32(D, kBM);
+            bool ok = nkv == 0 ||
+                      mbar_wait(smem_u32(&bars.q_ready), 0, wait_ns, status, kStatusTimeout);
+            // Slot descriptors: the ring's base plus slot * 32 KB (>> 4).  A
+            // K step (32 bytes: 16 halves or 8 fp32) sits (ks % 4) * 32 bytes
+            // into a 128-byte swizzled row, in box ks / 4 of its piece.  The
+            // 16-bit V tile is MN-major: its 64-column boxes are 16 KB apart
+            // (leading byte offset), 8-key groups 1024 bytes (stride), and a
+            // K step of 16 keys starts 2048 bytes further on.
+            const uint64_t dk0 = smem_desc(sR, 16, 1024, 2);
+            const uint64_t dv0 = k16 ? smem_desc(sR, kBoxBytes, 1024, 2) : dk0;
+            uint32_t load = 0;  // next load the MMAs consume
+            // S(0) and S(1) wait for their slots here; every later slot is
+            // covered by the go barrier of its step.
+            auto take = [&](uint32_t& slot, bool wait) {
+                slot = load % kSlots;
+                const bool got = !wait || mbar_wait(smem_u32(&bars.full[slot]), (load / kSlots) & 1,
+                                                    wait_ns, status, kStatusTimeout);
+                ++load;
+                if (got && wait) tc_fence_after();
+                return got;
             };
-            auto issue_pv = [&](int t, uint32_t j) {
-                // V tile is MN-major: 64-column boxes are kBN*128 bytes apart
-                // (leading byte offset), 8-key groups 1024 bytes apart (stride);
-                // K-step ks starts 16 keys (2048 bytes) further on.
-                const uint64_t b0 = (j % kStages) == 0 ? dv0 : dv1;
-                const uint32_t d = tmem + t * 256 + 128, a = tmem + t * 256;
-                const uint32_t acc0 = j > 0 ? 1u : 0u;
+            auto issue_s = [&](uint32_t j) {
+                const uint32_t d = tmem + (j & 1u) * kBK;
+                for (int p = 0; p < L::kPieces; ++p) {
+                    uint32_t slot;
+                    if (!take(slot, j < 2)) return false;
+                    const uint64_t b0 = dk0 + (uint64_t)(slot * (kSlotBytes / 16));
 #pragma unroll
-                for (int ks = 0; ks < kBN / 16; ++ks)
-                    mma_f16_ts(d, a + ks * 8, b0 + (uint64_t)(ks * (2048 / 16)), idesc_pv,
-                               ks > 0 ? 1u : acc0);
+                    for (int ks = 0; ks < L::kSSteps; ++ks) {
+                        const int k = p * L::kSSteps + ks;  // 32 bytes of the D columns per MMA
+                        mma_ts<OP>(d, tmem + L::kQCol + k * 8,
+                                   b0 + (uint64_t)((ks / 4) * (kBoxBytes / 16) + (ks % 4) * 2),
+                                   idesc_s, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&bars.empty[slot]));
+                }
+                mma_commit(smem_u32(&bars.s_full[j & 1u]));
+                return true;
             };
-            if (ok && n_kv_all > 0) {
-                ok = mbar_wait(smem_u32(&bars.k_full[0]), 0, wait_ns, status, kStatusTimeout);
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < kNQ; ++t)
-                        if (tile_n[t] > 0) issue_s(t, 0);
-                    mma_commit(smem_u32(&bars.k_empty[0]));
-                }
-            }
-            for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
-                const uint32_t st = j % kStages, ph = (j / kStages) & 1;
-                ok = mbar_wait(smem_u32(&bars.v_full[st]), ph, wait_ns, status, kStatusTimeout);
-                if (!ok) break;
-                bool k_next_ready = false;
-                const uint32_t jn = j + 1;
-                for (int t = 0; t < kNQ && ok; ++t) {
-                    if (j < tile_n[t]) {
-                        ok = mbar_wait(smem_u32(&bars.p_full[t]), j & 1, wait_ns, status, kStatusTimeout);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(t, j);
+            auto issue_pv = [&](uint32_t j) {
+                const uint32_t a = tmem + (j & 1u) * kBK, d = tmem + L::kOCol;
+                for (int p = 0; p < L::kPieces; ++p) {
+                    uint32_t slot;
+                    take(slot, false);
+                    const uint64_t b0 = dv0 + (uint64_t)(slot * (kSlotBytes / 16));
+#pragma unroll
+                    for (int ks = 0; ks < L::kVSteps; ++ks) {
+                        const int k = p * L::kVSteps + ks;  // 16 (16-bit) or 8 (TF32) keys per MMA
+                        const uint64_t boff =
+                            k16 ? (uint64_t)(ks * (2048 / 16))
+                                : (uint64_t)((ks / 4) * (L::kVBoxBytes / 16) + (ks % 4) * 2);
+                        mma_ts<OP>(d, a + k * 8, b0 + boff, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                     }
-                    if (jn < tile_n[t]) {
-                        if (!k_next_ready) {
-                            ok = mbar_wait(smem_u32(&bars.k_full[jn % kStages]),
-                                           (jn / kStages) & 1, wait_ns, status, kStatusTimeout);
-                            if (!ok) break;
-                            tc_fence_after();
-                            k_next_ready = true;
-                        }
-                        issue_s(t, jn);
-                    }
+                    mma_commit(smem_u32(&bars.empty[slot]));
                 }
+                // The last step's softmax rescales O only after this group
+                // (S(j+2), whose completion tells the other steps, does not exist).
+                if (j + 2 == nkv) mma_commit(smem_u32(&bars.pv_last));
+            };
+            if (ok && nkv > 0) ok = issue_s(0);
+            if (ok && nkv > 1) ok = issue_s(1);
+            for (uint32_t j = 0; j < nkv && ok; ++j) {
+                ok = mbar_wait(smem_u32(&bars.go[j & 1u]), (j >> 1) & 1, wait_ns, status,
+                               kStatusTimeout);
                 if (!ok) break;
-                mma_commit(smem_u32(&bars.v_empty[st]));
-                if (k_next_ready) mma_commit(smem_u32(&bars.k_empty[jn % kStages]));
+                tc_fence_after();
+                issue_pv(j);
+                if (j + 2 < nkv) issue_s(j + 2);
             }
             if (!ok) record_timeout(status, &bars);
             // Wait until every MMA this thread issued has completed.
             mma_commit(smem_u32(&bars.mma_done));
             mbar_wait(smem_u32(&bars.mma_done), 0, kDrainWaitNs);
         }
+    } else if (warp == kGateWarp) {
+        // ------------------------------------------------------------ gate
+        // Step j's MMAs read the loads of V(j), then those of K(j+2), in
+        // load order; S(0) and S(1) took the first ones.  go(j) reuses the
+        // barrier of step j - 2, whose phase must complete first (its P
+        // arrivals precede this step's, so none can land in the old phase).
+        if (lane == 0) {
+            uint32_t load = (uint32_t)L::kPieces * min(nkv, 2u);
+            bool ok = true;
+            for (uint32_t j = 0; j < nkv && ok; ++j) {
+                if (j >= 2)
+                    ok = mbar_wait(smem_u32(&bars.go[j & 1u]), ((j - 2) >> 1) & 1, wait_ns, status,
+                                   kStatusTimeout);
+                const uint32_t n = (uint32_t)L::kPieces * (j + 2 < nkv ? 2u : 1u);
+                for (uint32_t i = 0; i < n && ok; ++i, ++load)
+                    ok = mbar_wait(smem_u32(&bars.full[load % kSlots]), (load / kSlots) & 1, wait_ns,
+                                   status, kStatusTimeout);
+                if (!ok) break;
+                mbar_arrive(smem_u32(&bars.go[j & 1u]));
+            }
+            if (!ok) record_timeout(status, &bars);
+        }
     } else {
         // ------------------------------------------------------------ softmax
-        const int t = warp / 4;                 // query tile of this warpgroup
-        const int wq = warp % 4;                // TMEM lane quarter
-        const uint32_t row_in_tile = wq * 32 + lane;
-        const uint32_t row = (qt0 + t) * kBM + row_in_tile;
-        const uint32_t t_s = tmem + t * 256 + ((uint32_t)(wq * 32) << 16);
-        const uint32_t t_o = t_s + 128;
+        const uint32_t row_in_tile = warp * 32 + lane;
+        const uint32_t row = tile_row0 + row_in_tile;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_o = lane_base + L::kOCol;
+        const uint32_t sw = row_in_tile & 7u;
         bool ok = true;
-        // ---- prologue: round the staged fp32 query tiles to fp16/bf16 into
-        // the MMA's 128-byte swizzled K-major layout (all eight warps, one
-        // tile after the other: thread = row wq*32+lane, half the columns per
-        // warpgroup), checking the fp16 range like the pre-pass does for K, V.
-        {
-            const uint32_t qr = row_in_tile;             // row converted by this thread
-            const uint32_t sw = qr & 7u;
-
-            bool overflow = false;
-            for (int tq = 0; tq < kNQ; ++tq) {
-                ok = ok && mbar_wait(smem_u32(&bars.q_staged[tq]), 0, wait_ns, status, kStatusTimeout);
-                if (ok) {
-                    const uint8_t* q32 = smem + L::q32_off(tq);
-                    uint8_t* q16 = smem + L::kQOff + tq * L::kQTileBytes;
+        // ---- prologue: the query row from the fp32 staging boxes into TMEM
+        // (16-bit: rounded and packed in pairs, fp16 range checked).
+        if (nkv > 0) {
+            ok = mbar_wait(smem_u32(&bars.q_full), 0, wait_ns, status, kStatusTimeout);
+            if (__any_sync(0xffffffffu, !ok)) ok = false;
+            if (ok) {
+                const uint8_t* stage = smem + L::kQStageSlot * kSlotBytes;
+                bool overflow = false;
 #pragma unroll
-                    for (uint32_t c = (uint32_t)t * (D / 16); c < (uint32_t)(t + 1) * (D / 16); ++c) {
-                        // fp16 chunk c = columns 8c..8c+7 = fp32 chunks 2c, 2c+1
-                        const uint32_t k0 = 2 * c, k1 = 2 * c + 1;
-                        const float4 a = *reinterpret_cast<const float4*>(
-                            q32 + (k0 / 8) * L::kOBoxBytes + qr * 128 + (((k0 % 8) ^ sw) * 16));
-                        const float4 b = *reinterpret_cast<const float4*>(
-                            q32 + (k1 / 8) * L::kOBoxBytes + qr * 128 + (((k1 % 8) ^ sw) * 16));
-                        if (!BF16) {
-                            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-                            overflow |= !(mx <= 65504.f);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    const uint8_t* box_row = stage + c * kBoxBytes + row_in_tile * 128;
+#pragma unroll
+                    for (uint32_t q4 = 0; q4 < 8; ++q4) {
+                        const uint4 v4 = *reinterpret_cast<const uint4*>(box_row + ((q4 ^ sw) * 16));
+                        r[4 * q4] = v4.x;
+                        r[4 * q4 + 1] = v4.y;
+                        r[4 * q4 + 2] = v4.z;
+                        r[4 * q4 + 3] = v4.w;
+                    }
+                    if constexpr (k16) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float a = __uint_as_float(r[2 * i]), b = __uint_as_float(r[2 * i + 1]);
+                            if (!kBf16) overflow |= !(fmaxf(fabsf(a), fabsf(b)) <= 65504.f);
+                            pk[i] = pack_half2(a, b, kBf16);
                         }
-                        uint4 out;
-                        out.x = pack_half2(a.x, a.y, BF16);
-                        out.y = pack_half2(a.z, a.w, BF16);
-                        out.z = pack_half2(b.x, b.y, BF16);
-                        out.w = pack_half2(b.z, b.w, BF16);
-                        *reinterpret_cast<uint4*>(q16 + (c / 8) * (kBM * 128) + qr * 128 +
-                                                  (((c % 8) ^ sw) * 16)) = out;
+                        tmem_st16(lane_base + L::kQCol + c * 16, pk);
+                    } else {
+                        tmem_st32(lane_base + L::kQCol + c * 32, r);
                     }
                 }
-                // Generic-proxy reads and writes of the staging and of the Q
-                // tile are ordered before the next TMA write and the MMAs.
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&bars.q_ready[tq]));
+                tmem_wait_st();
+                if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicOr(status, kStatusRange);
             }
-            if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicOr(status, kStatusRange);
+            // The staging reads come before the TMA writes that reuse the
+            // slots, the TMEM stores before the MMAs that read them.
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.q_ready));
         }
         float m_used = -CUDART_INF_F;  // log2 units
         float l_sum = 0.f;
-        const uint32_t nkv = tile_n[t];
-        for (uint32_t j = 0; j < nkv; ++j) {
-            ok = mbar_wait(smem_u32(&bars.s_full[t]), j & 1, wait_ns, status, kStatusTimeout);
-            const bool any_fail = __any_sync(0xffffffffu, !ok);
-            if (any_fail) { ok = false; break; }
+        for (uint32_t j = 0; j < nkv && ok; ++j) {
+            const uint32_t buf = j & 1u;
+            ok = mbar_wait(smem_u32(&bars.s_full[buf]), (j >> 1) & 1, wait_ns, status, kStatusTimeout);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             tc_fence_after();
-            float s[kBN];
+            const uint32_t t_s = lane_base + buf * kBK;
+            float s[kBK];
             {
-                uint32_t r[kBN];
+                uint32_t r[kBK];
                 tmem_ld128_sync(t_s, r);
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(r[i]);
+                for (int i = 0; i < kBK; ++i) s[i] = __uint_as_float(r[i]);
             }
-            if (j0 + j + 1 == n_kv[t]) {  // diagonal tile: keys above the row are not attended
-                const uint32_t key0 = (j0 + j) * kBN;
+            const uint32_t key0 = (j0 + j) * kBK;
+            if (key0 + kBK > tile_row0) {  // the diagonal block: keys above the row are not attended
 #pragma unroll
-                for (int c = 0; c < kBN; ++c)
+                for (int c = 0; c < kBK; ++c)
                     if (key0 + c > row) s[c] = -CUDART_INF_F;
             }
-            // Row max as 8 independent chains (a single 128-long chain of
-            // dependent max operations would sit on the ping-pong's critical path).
+            // Row max as 8 independent chains.
             float mx8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx8[i] = s[i];
 #pragma unroll
-            for (int c = 8; c < kBN; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], s[c]);
-            float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            for (int c = 8; c < kBK; ++c) mx8[c % 8] = fmaxf(mx8[c % 8], s[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
             const float m_new = mx * scale_log2;
             float corr = 1.f;
             bool rescale = false;
             if (m_new > m_used + kRescaleThreshold) {
-                corr = ex2(m_used - m_new);      // 0 on the first tile
+                corr = ex2(m_used - m_new);      // 0 on the first step
                 rescale = (j > 0);
                 m_used = m_new;
             }
-            const float neg_m = -m_used;
+            // A row with no attended key so far (every score -inf) keeps its
+            // weights at exactly 0 instead of forming -inf - (-inf).
+            const float neg_m = m_used == -CUDART_INF_F ? 0.f : -m_used;
             // exponent arguments two at a time (packed fp32x2), row sum as four
             // independent packed accumulators
             const float2 sc2 = make_float2(scale_log2, scale_log2);
@@ -475,22 +506,51 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t pk[16];
+            for (int c = 0; c < kBK / 32; ++c) {
+                if constexpr (k16) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float2 x = __ffma2_rn(
-                        make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2, nm2);
-                    const float p0 = ex2(x.x), p1 = ex2(x.y);
-                    acc[i % 4] = __fadd2_rn(acc[i % 4], make_float2(p0, p1));
-                    pk[i] = pack_half2(p0, p1, BF16);
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 x = __ffma2_rn(
+                            make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2, nm2);
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        acc[i % 4] = __fadd2_rn(acc[i % 4], make_float2(p0, p1));
+                        pk[i] = pack_half2(p0, p1, kBf16);
+                    }
+                    tmem_st16(t_s + c * 16, pk);
+                } else {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 x = __ffma2_rn(
+                            make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2, nm2);
+                        // The MMA reads the weights' top 19 bits; the row sum takes
+                        // the same truncated values, so the output is an exact
+                        // convex combination of the weights the MMA used.
+                        const uint32_t b0 = __float_as_uint(ex2(x.x)) & kTf32Mask;
+                        const uint32_t b1 = __float_as_uint(ex2(x.y)) & kTf32Mask;
+                        acc[i % 4] = __fadd2_rn(acc[i % 4],
+                                                make_float2(__uint_as_float(b0), __uint_as_float(b1)));
+                        pk[2 * i] = b0;
+                        pk[2 * i + 1] = b1;
+                    }
+                    tmem_st32(t_s + c * 32, pk);
                 }
-                tmem_st16(t_s + c * 16, pk);
             }
             const float rowsum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) +
                                  ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
             l_sum = fmaf(l_sum, corr, rowsum);
             if (__any_sync(0xffffffffu, rescale)) {
+                // O holds every P.V up to step j-1 once P.V(j-1) has completed:
+                // S(j+1) was issued right after it, and the last step has its
+                // own barrier.  (Waiting on S(j+1) here consumes the same phase
+                // the next step waits for.)
+                ok = j + 1 < nkv ? mbar_wait(smem_u32(&bars.s_full[buf ^ 1u]), ((j + 1) >> 1) & 1,
+                                             wait_ns, status, kStatusTimeout)
+                                 : mbar_wait(smem_u32(&bars.pv_last), 0, wait_ns, status,
+                                             kStatusTimeout);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                tc_fence_after();
                 const float f = rescale ? corr : 1.f;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -503,39 +563,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(smem_u32(&bars.p_full[t]));
+            mbar_arrive(smem_u32(&bars.go[buf]));
         }
-        // ---- epilogue.  After the CTA's last MMA the K/V ring is free: each
-        // thread writes its row of O (normalised, or this chunk's unnormalised
-        // partial) into the swizzled staging boxes, and one thread of the
-        // warpgroup stores the tile with TMA (whole 128-byte lines; rows past
-        // m are clipped by the tensor map).
+        // ---- epilogue: O (normalised, or this chunk's unnormalised partial)
+        // into the ring's first slots, then TMA stores of whole lines.
         const bool split_item = n_chunks > 1;
         if (ok && nkv > 0) {
             ok = mbar_wait(smem_u32(&bars.mma_done), 0, wait_ns, status, kStatusTimeout);
             if (__any_sync(0xffffffffu, !ok)) ok = false;
         }
-        uint8_t* stage = smem + L::kStageOff + t * L::kOTileBytes;
+        uint8_t* stage = smem;
         if (ok && nkv > 0) {
             tc_fence_after();
             const float scale_o = split_item ? 1.f : 1.0f / l_sum;
-            const uint32_t sw = row_in_tile & 7u;
-            // the whole row of O in one TMEM load (one wait)
-            uint32_t r[D];
-            if constexpr (D == 128) {
-                tmem_ld128_sync(t_o, r);
-            } else {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-                    tmem_ld32(t_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
-                tmem_wait_ld();
-            }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                uint8_t* box_row = stage + c * L::kOBoxBytes + row_in_tile * 128;
+                uint32_t r[32];
+                tmem_ld32_sync(t_o + c * 32, r);
+                uint8_t* box_row = stage + c * kBoxBytes + row_in_tile * 128;
 #pragma unroll
                 for (uint32_t q4 = 0; q4 < 8; ++q4) {
-                    const uint32_t i = c * 32 + 4 * q4;
+                    const uint32_t i = 4 * q4;
                     const float4 v4 = make_float4(__uint_as_float(r[i]) * scale_o,
                                                   __uint_as_float(r[i + 1]) * scale_o,
                                                   __uint_as_float(r[i + 2]) * scale_o,
@@ -549,12 +597,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             fence_proxy_async_smem();
         }
-        named_barrier(1 + t, 128);
-        if (ok && nkv > 0 && wq == 0 && lane == 0) {
-            const int32_t y0 = (int32_t)((qt0 + t) * kBM);
+        named_barrier(1, kSoftmaxThreads);
+        if (ok && nkv > 0 && warp == 0 && lane == 0) {
+            const int32_t y0 = (int32_t)tile_row0;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                const uint32_t src = smem_u32(stage + c * L::kOBoxBytes);
+                const uint32_t src = smem_u32(stage + c * kBoxBytes);
                 if (split_item)
                     tma_store_2d(&tm_po, src, c * 32,
                                  (int32_t)((chunk * num_q_heads + h) * split.m_pad) + y0);
@@ -575,50 +623,51 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
-// fp32 -> fp16/bf16 rounding pre-pass for the keys and values: k [m,
-// kv_stride] -> kh [m, hkv*d], likewise v (the queries are rounded inside the
-// prefill kernel, each tile once).  grid.y selects the tensor (0 = k, 1 = v).
-// Each thread converts 8 consecutive elements of one row (two 128-bit loads,
-// one 128-bit store).
-template <bool BF16>
-__global__ void round_operands_kernel(const float* __restrict__ k, const float* __restrict__ v,
-                                      uint16_t* __restrict__ kh, uint16_t* __restrict__ vh,
-                                      uint32_t m, uint32_t kv_cols, uint32_t kv_stride,
-                                      unsigned int* status) {
-    // Launched as a programmatic dependent of the kernel before it: wait for
-    // that grid before any global access.  Only then may the prefill kernel
-    // launch (it stages the caller's Q before its own wait, so every kernel
-    // before this one must have completed); it reads the rounded K and V
-    // only after this grid has completed.
+// TF32 pre-pass: K rounded to nearest TF32 into kr [m, kv_cols] (grid.y = 0,
+// eight elements per thread), and V rounded and transposed into
+// vt [kv_cols, m4] (grid.y = 1, 32 x 32 tiles through shared memory: rows of
+// V in, rows of V^T out, both as whole 128-byte lines).
+__global__ void __launch_bounds__(256)
+round_transpose_tf32_kernel(const float* __restrict__ k, const float* __restrict__ v,
+                            float* __restrict__ kr, float* __restrict__ vt, uint32_t m,
+                            uint32_t kv_cols, uint32_t kv_stride, uint32_t m4) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const float* src = blockIdx.y == 0 ? k : v;
-    uint16_t* dst = blockIdx.y == 0 ? kh : vh;
-    const uint32_t cols = kv_cols;
-    const uint32_t stride = kv_stride;
-    const uint32_t per_row = cols / 8;
-    const size_t total = (size_t)m * per_row;
-    bool overflow = false;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (size_t)gridDim.x * blockDim.x) {
-        const size_t r = i / per_row;
-        const uint32_t c = (uint32_t)(i % per_row) * 8;
-        const float4* s4 = reinterpret_cast<const float4*>(src + r * stride + c);
-        const float4 a = __ldcs(s4), b = __ldcs(s4 + 1);
-        uint4 out;
-        out.x = pack_half2(a.x, a.y, BF16);
-        out.y = pack_half2(a.z, a.w, BF16);
-        out.z = pack_half2(b.x, b.y, BF16);
-        out.w = pack_half2(b.z, b.w, BF16);
-        if (!BF16) {
-            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-            overflow |= !(mx <= 65504.f);
+    if (blockIdx.y == 0) {
+        const uint32_t per_row = kv_cols / 8;
+        const size_t total = (size_t)m * per_row;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+             i += (size_t)gridDim.x * blockDim.x) {
+            const size_t r = i / per_row;
+            const uint32_t c = (uint32_t)(i % per_row) * 8;
+            const float4* s4 = reinterpret_cast<const float4*>(k + r * kv_stride + c);
+            float4 a = __ldcs(s4), b = __ldcs(s4 + 1);
+            a = make_float4(round_tf32(a.x), round_tf32(a.y), round_tf32(a.z), round_tf32(a.w));
+            b = make_float4(round_tf32(b.x), round_tf32(b.y), round_tf32(b.z), round_tf32(b.w));
+            float4* d4 = reinterpret_cast<float4*>(kr + r * kv_cols + c);
+            d4[0] = a;
+            d4[1] = b;
         }
-        *reinterpret_cast<uint4*>(dst + r * cols + c) = out;
+        return;
     }
-    if (__any_sync(0xffffffffu, overflow) && (threadIdx.x % 32) == 0)
-        atomicOr(status, kStatusRange);
+    __shared__ float tile[32][33];
+    const uint32_t tx = threadIdx.x % 32, ty = threadIdx.x / 32;  // 32 x 8 threads
+    const uint32_t key_tiles = (m + 31) / 32, col_tiles = kv_cols / 32;
+    for (uint32_t tid = blockIdx.x; tid < key_tiles * col_tiles; tid += gridDim.x) {
+        const uint32_t j0 = (tid / col_tiles) * 32, c0 = (tid % col_tiles) * 32;
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) {
+            const uint32_t j = j0 + ty + 8 * i;
+            tile[ty + 8 * i][tx] = j < m ? round_tf32(__ldcs(v + (size_t)j * kv_stride + c0 + tx)) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) {
+            const uint32_t c = c0 + ty + 8 * i, j = j0 + tx;
+            if (j < m4) vt[(size_t)c * m4 + j] = tile[tx][ty + 8 * i];
+        }
+        __syncthreads();
+    }
 }
 
 __global__ void wait_timeout_selftest_kernel(unsigned int* status, uint64_t wait_ns) {
@@ -632,67 +681,74 @@ __global__ void wait_timeout_selftest_kernel(unsigned int* status, uint64_t wait
     if (!mbar_wait(smem_u32(&bar), 0, wait_ns, status, kStatusTimeout)) atomicOr(status, kStatusTimeout);
 }
 
-// fp16/bf16 operand map: tight rows of `cols` elements, boxes of 64
-// elements (128 bytes) x box_rows, 128-byte swizzle.
-bool encode_operand_map(CUtensorMap* map, const void* base, uint32_t cols, uint32_t rows,
-                        uint32_t box_rows, bool bf16) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t gdim[2] = {cols, rows};
-    cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estride[2] = {1, 1};
-    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                     2, const_cast<void*>(base), gdim, gstride, box, estride,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+// Workspace: the rounded K and V (TF32: K rounded, V rounded and transposed
+// with rows of m4 keys), each 256-byte aligned, then the split partials.
+struct OperandBytes {
+    size_t k_bytes, v_bytes;
+    uint32_t m4;
+};
+
+OperandBytes operand_bytes(uint32_t m, uint32_t num_kv_heads, uint32_t head_dim, bool tf32) {
+    OperandBytes w{};
+    w.m4 = (m + 3) / 4 * 4;
+    const size_t elem = tf32 ? 4 : 2;
+    w.k_bytes = align256((size_t)m * num_kv_heads * head_dim * elem);
+    w.v_bytes = tf32 ? align256((size_t)num_kv_heads * head_dim * w.m4 * 4) : w.k_bytes;
+    return w;
 }
 
-// Workspace bytes of the rounded fp16/bf16 K and V (each 256-byte aligned).
-size_t operand_bytes_16(uint32_t m, uint32_t num_kv_heads, uint32_t head_dim) {
-    return 2 * align256((size_t)m * num_kv_heads * head_dim * 2);
-}
-
-template <int D, bool BF16>
+template <int D, Op OP>
 cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, uint32_t m,
                       uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t q_stride,
                       uint32_t kv_stride, float scale, void* workspace, unsigned int* status,
                       uint64_t wait_ns, cudaStream_t stream) {
-    using L = TcLayout<D>;
-    const PrefillPlan plan = make_plan(m, num_q_heads, D, device_sm_count(), 1, kNQ);
-    const size_t operand_bytes = operand_bytes_16(m, num_kv_heads, D);
+    using L = TcLayout<D, OP>;
+    constexpr bool kTf32 = OP == Op::TF32;
+    const PrefillPlan plan = make_plan(m, num_q_heads, D, device_sm_count(), kPerQ, 1);
+    const OperandBytes w = operand_bytes(m, num_kv_heads, D, kTf32);
     const uint32_t q_cols = num_q_heads * D, kv_cols = num_kv_heads * D;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint16_t* kh = reinterpret_cast<uint16_t*>(ws);
-    uint16_t* vh = reinterpret_cast<uint16_t*>(ws + align256((size_t)m * kv_cols * 2));
+    void* kw = ws;
+    void* vw = ws + w.k_bytes;
     SplitArgs split = plan.split;
-    split.part_o = reinterpret_cast<float*>(ws + operand_bytes);
-    split.part_ml = reinterpret_cast<float*>(ws + operand_bytes + plan.part_o_bytes);
+    split.part_o = reinterpret_cast<float*>(ws + w.k_bytes + w.v_bytes);
+    split.part_ml = reinterpret_cast<float*>(ws + w.k_bytes + w.v_bytes + plan.part_o_bytes);
 
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     {
-        const size_t work = (size_t)m * kv_cols / 8;
-        const uint32_t threads = 256;
-        uint32_t blocks = (uint32_t)std::min<size_t>((work + threads - 1) / threads, 4096);
-        cudaLaunchAttribute pattr[1];
-        pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        pattr[0].val.programmaticStreamSerializationAllowed = 1;
+        const size_t k_work = (size_t)m * kv_cols / 8;
+        const size_t v_work = kTf32 ? (size_t)((m + 31) / 32) * (kv_cols / 32) : 0;
+        const uint32_t blocks =
+            (uint32_t)std::min<size_t>(std::max<size_t>((k_work + 255) / 256, v_work), 4096);
         cudaLaunchConfig_t pcfg = {};
         pcfg.gridDim = dim3(blocks, 2, 1);
-        pcfg.blockDim = dim3(threads, 1, 1);
+        pcfg.blockDim = dim3(256, 1, 1);
         pcfg.stream = stream;
-        pcfg.attrs = pattr;
+        pcfg.attrs = attr;
         pcfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&pcfg, round_operands_kernel<BF16>, k, v, kh, vh, m,
-                                           kv_cols, kv_stride, status);
+        cudaError_t e;
+        if constexpr (kTf32)
+            e = cudaLaunchKernelEx(&pcfg, round_transpose_tf32_kernel, k, v,
+                                   static_cast<float*>(kw), static_cast<float*>(vw), m, kv_cols,
+                                   kv_stride, w.m4);
+        else
+            e = cudaLaunchKernelEx(&pcfg, round_operands_kernel<OP == Op::BF16>, k, v,
+                                   static_cast<uint16_t*>(kw), static_cast<uint16_t*>(vw), m,
+                                   kv_cols, kv_stride, status);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap tq, tk, tv, to, tpo;
-    if (!encode_output_map(&tq, q, q_cols, m, q_stride, kBM) ||
-        !encode_operand_map(&tk, kh, kv_cols, m, kBN, BF16) ||
-        !encode_operand_map(&tv, vh, kv_cols, m, kBN, BF16) ||
-        !encode_output_map(&to, o, q_cols, m, q_stride, kBM))
-        return cudaErrorNotSupported;
+    bool maps = encode_output_map(&tq, q, q_cols, m, q_stride, kBM) &&
+                encode_output_map(&to, o, q_cols, m, q_stride, kBM);
+    if constexpr (kTf32)
+        maps = maps && encode_output_map(&tk, kw, kv_cols, m, kv_cols, kBK) &&
+               encode_output_map(&tv, vw, m, kv_cols, w.m4, D);
+    else
+        maps = maps && encode_operand_map(&tk, kw, kv_cols, m, kBK, OP == Op::BF16) &&
+               encode_operand_map(&tv, vw, kv_cols, m, kBK, OP == Op::BF16);
+    if (!maps) return cudaErrorNotSupported;
     if (split.kv_chunk != kNoSplit) {
         if (!encode_output_map(&tpo, split.part_o, D,
                                (uint64_t)split.n_chunks_max * num_q_heads * split.m_pad, D, kBM))
@@ -700,14 +756,10 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     } else {
         tpo = to;  // not used without a split
     }
-
     {
-        const cudaError_t e = ensure_dynamic_smem<prefill_tc_kernel<D, BF16>>((int)L::kSmemAlloc);
+        const cudaError_t e = ensure_dynamic_smem<prefill_tc_kernel<D, OP>>((int)L::kSmemAlloc);
         if (e != cudaSuccess) return e;
     }
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.n_items * num_q_heads, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -715,7 +767,7 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, BF16>, tq, tk, tv, to, tpo, m,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, OP>, tq, tk, tv, to, tpo, m,
                                        num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e,
                                        status, wait_ns, split);
     if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;
@@ -730,12 +782,46 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     return cudaLaunchKernelEx(&ccfg, prefill_combine_kernel<D>, split, o, m, num_q_heads, q_stride);
 }
 
+template <Op OP>
+cudaError_t launch_d(const float* q, const float* k, const float* v, float* o, uint32_t m,
+                     uint32_t num_q_heads, uint32_t num_kv_heads, uint32_t head_dim,
+                     uint32_t q_stride, uint32_t kv_stride, float scale, void* workspace,
+                     unsigned int* status, uint64_t wait_ns, cudaStream_t stream) {
+    if (head_dim == 128)
+        return launch_tc<128, OP>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
+                                  scale, workspace, status, wait_ns, stream);
+    if (head_dim == 64)
+        return launch_tc<64, OP>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, kv_stride,
+                                 scale, workspace, status, wait_ns, stream);
+    return cudaErrorInvalidValue;
+}
+
+size_t workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                       uint32_t head_dim, bool tf32) {
+    const PrefillPlan p = make_plan(m, num_q_heads, head_dim, device_sm_count(), kPerQ, 1);
+    const OperandBytes w = operand_bytes(m, num_kv_heads, head_dim, tf32);
+    return w.k_bytes + w.v_bytes + p.part_o_bytes + p.part_ml_bytes;
+}
+
 }  // namespace
+
+// Pairs of query tiles halve the loads and hand-offs per MMA, single tiles
+// balance a small grid better: pairs once they fill the SMs twice over.
+bool prefill_use_pairs(uint32_t m, uint32_t num_q_heads, int sm_count) {
+    const uint64_t pairs = (m + 2 * kBM - 1) / (2 * kBM);
+    return pairs * num_q_heads >= 2 * (uint64_t)std::max(sm_count, 1);
+}
 
 size_t prefill_tc_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim) {
-    const PrefillPlan p = make_plan(m, num_q_heads, head_dim, device_sm_count(), 1, kNQ);
-    return operand_bytes_16(m, num_kv_heads, head_dim) + p.part_o_bytes + p.part_ml_bytes;
+    if (prefill_use_pairs(m, num_q_heads, device_sm_count()))
+        return prefill_pair_workspace_bytes(m, num_q_heads, num_kv_heads, head_dim);
+    return workspace_bytes(m, num_q_heads, num_kv_heads, head_dim, false);
+}
+
+size_t prefill_tf32_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                    uint32_t head_dim) {
+    return workspace_bytes(m, num_q_heads, num_kv_heads, head_dim, true);
 }
 
 cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, float* o,
@@ -743,19 +829,22 @@ cudaError_t launch_prefill_tc(const float* q, const float* k, const float* v, fl
                               uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
                               float scale, bool bf16, void* workspace, unsigned int* status,
                               uint64_t wait_ns, cudaStream_t stream) {
-#define ATTN_TC_CASE(DD)                                                                     \
-    if (head_dim == DD) {                                                                    \
-        return bf16 ? launch_tc<DD, true>(q, k, v, o, m, num_q_heads, num_kv_heads, q_stride, \
-                                          kv_stride, scale, workspace, status, wait_ns,       \
-                                          stream)                                            \
-                    : launch_tc<DD, false>(q, k, v, o, m, num_q_heads, num_kv_heads,          \
-                                           q_stride, kv_stride, scale, workspace, status,     \
-                                           wait_ns, stream);                                 \
-    }
-    ATTN_TC_CASE(64)
-    ATTN_TC_CASE(128)
-#undef ATTN_TC_CASE
-    return cudaErrorInvalidValue;
+    if (prefill_use_pairs(m, num_q_heads, device_sm_count()))
+        return launch_prefill_pair(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_stride,
+                                   kv_stride, scale, bf16, workspace, status, wait_ns, stream);
+    return bf16 ? launch_d<Op::BF16>(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_stride,
+                                     kv_stride, scale, workspace, status, wait_ns, stream)
+                : launch_d<Op::FP16>(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_stride,
+                                     kv_stride, scale, workspace, status, wait_ns, stream);
+}
+
+cudaError_t launch_prefill_tf32(const float* q, const float* k, const float* v, float* o,
+                                uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
+                                uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
+                                float scale, void* workspace, unsigned int* status,
+                                uint64_t wait_ns, cudaStream_t stream) {
+    return launch_d<Op::TF32>(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_stride,
+                              kv_stride, scale, workspace, status, wait_ns, stream);
 }
 
 cudaError_t launch_wait_timeout_selftest(unsigned int* status, uint64_t limit_ns) {

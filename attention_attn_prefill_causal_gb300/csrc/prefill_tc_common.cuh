@@ -15,6 +15,9 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -130,6 +133,55 @@ prefill_combine_kernel(const SplitArgs split, float* __restrict__ o, uint32_t m,
     dst[1] = make_float4(O[4] * inv, O[5] * inv, O[6] * inv, O[7] * inv);
 }
 
+__device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16) {
+    if (bf16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 16-bit pre-pass: k [m, kv_stride] -> kh [m, kv_cols] rounded to fp16/bf16
+// (grid.y = 0), likewise v (grid.y = 1).  Each thread converts 8 consecutive
+// elements of one row (two 128-bit loads, one 128-bit store).
+template <bool BF16>
+__global__ void __launch_bounds__(256)
+round_operands_kernel(const float* __restrict__ k, const float* __restrict__ v,
+                      uint16_t* __restrict__ kh, uint16_t* __restrict__ vh, uint32_t m,
+                      uint32_t kv_cols, uint32_t kv_stride, unsigned int* status) {
+    // A programmatic dependent of the kernel before it: wait for that grid
+    // before any global access, then let the prefill kernel launch (it reads
+    // kh and vh only after this grid has completed).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const float* src = blockIdx.y == 0 ? k : v;
+    uint16_t* dst = blockIdx.y == 0 ? kh : vh;
+    const uint32_t per_row = kv_cols / 8;
+    const size_t total = (size_t)m * per_row;
+    bool overflow = false;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / per_row;
+        const uint32_t c = (uint32_t)(i % per_row) * 8;
+        const float4* s4 = reinterpret_cast<const float4*>(src + r * kv_stride + c);
+        const float4 a = __ldcs(s4), b = __ldcs(s4 + 1);
+        uint4 out;
+        out.x = pack_half2(a.x, a.y, BF16);
+        out.y = pack_half2(a.z, a.w, BF16);
+        out.z = pack_half2(b.x, b.y, BF16);
+        out.w = pack_half2(b.z, b.w, BF16);
+        if (!BF16) {
+            const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                                   fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+            overflow |= !(mx <= 65504.f);
+        }
+        *reinterpret_cast<uint4*>(dst + r * kv_cols + c) = out;
+    }
+    if (__any_sync(0xffffffffu, overflow) && (threadIdx.x % 32) == 0)
+        atomicOr(status, kStatusRange);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -163,6 +215,23 @@ bool encode_output_map(CUtensorMap* map, const void* base, uint64_t cols, uint64
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// fp16/bf16 operand map: tight rows of `cols` elements, boxes of 64
+// elements (128 bytes) x box_rows, 128-byte swizzle.
+bool encode_operand_map(CUtensorMap* map, const void* base, uint32_t cols, uint32_t rows,
+                        uint32_t box_rows, bool bf16) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     2, const_cast<void*>(base), gdim, gstride, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 struct PrefillPlan {
     uint32_t n_items;          // work items per head (pairs, or pair chunks)

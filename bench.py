@@ -325,20 +325,28 @@ def remainder_graphs(bench, stream, append=True):
 TF32_PEAK_RATIO = 1.1 / 2.25
 
 
-def prefill_launches(m, num_q_heads, sms, tiles_per_item=2):
+def prefill_launches(m, num_q_heads, sms, tf32=False):
     """Kernels one tensor-core prefill call launches: the rounding pre-pass
     and the main kernel, plus the combine kernel when the call splits its key
-    walk.  Mirrors the library's split plan: a work item is a pair of
-    128-row query tiles (fp16/bf16 kernel) or one tile (TF32 kernel); split
-    only when items x heads leave SMs idle, with the smallest chunk whose
-    items fit in one wave."""
+    walk.  Mirrors the library's plan: 16-bit calls whose query-tile pairs
+    fill the SMs twice over run the pair kernel (a work item is two 128-row
+    query tiles), the others and every TF32 call the single-tile kernel (one
+    tile); the key walk is split only when items x heads leave SMs idle, with
+    the smallest chunk whose items fit in one wave."""
     n_qt = -(-m // 128)
+    pairs = -(-m // 256)
+    tiles_per_item = 2 if (not tf32 and pairs * num_q_heads >= 2 * sms) else 1
     n_units = -(-m // (128 * tiles_per_item))
 
     def nk(u):
         return min(tiles_per_item * u + tiles_per_item, n_qt)
     if n_units == 0 or n_units * num_q_heads >= sms:
         return 2
+    nk_last = nk(n_units - 1)
+    for c in range(2, nk_last):
+        if sum(-(-nk(u) // c) for u in range(n_units)) * num_q_heads <= sms:
+            return 3
+    return 2
     nk_last = nk(n_units - 1)
     for c in range(2, nk_last):
         if sum(-(-nk(u) // c) for u in range(n_units)) * num_q_heads <= sms:
@@ -366,7 +374,7 @@ class PrefillBench:
         # call splits its key walk, the partials that a third kernel merges.
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         self.launches_per_call = prefill_launches(
-            shape.m, shape.num_q_heads, sms, 1 if self.prec == attn.ATTN_PREC_TF32 else 2)
+            shape.m, shape.num_q_heads, sms, self.prec == attn.ATTN_PREC_TF32)
 
     def call(self, i, stream):
         c, a, r = self.c, self.attn, i % self.R

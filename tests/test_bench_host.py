@@ -94,7 +94,7 @@ def test_prefill_launch_count_follows_the_library_plan(m, hq, hkv, d):
     operands16 = 2 * (-(-m * hkv * d * 2 // 256) * 256)
     wst = attn.attn_prefill_workspace_size(m, hq, hkv, d, attn.ATTN_PREC_TF32)
     operandst = -(-m * hkv * d * 4 // 256) * 256 + -(-hkv * d * (-(-m // 4) * 4) * 4 // 256) * 256
-    launches16 = bench.prefill_launches(m, hq, 152, 2)   # pairs of query tiles
-    launchest = bench.prefill_launches(m, hq, 152, 1)    # single query tiles
+    launches16 = bench.prefill_launches(m, hq, 152)             # pair or single-tile kernel
+    launchest = bench.prefill_launches(m, hq, 152, tf32=True)   # single query tiles
     assert (ws16 > operands16) == (launches16 == 3), (ws16, operands16, launches16)
     assert (wst > operandst) == (launchest == 3), (wst, operandst, launchest)
