@@ -20,7 +20,7 @@
 //
 // CTA work unit: two consecutive 128-row query tiles (A = rows q0..q0+127,
 // B = q0+128..q0+255) of one head; keys are walked in 128-row tiles up to the
-// diagonal.  Warp roles (320 threads):
+// diagonal.  Warp roles (352 threads):
 //   warps 0-3  softmax for tile A  (thread r owns TMEM lane r = query row r)
 //   warps 4-7  softmax for tile B
 //   warp  8    TMA producer: both fp32 Q tiles once (staged in the K and
@@ -28,6 +28,18 @@
 //              into the fp16 Q tiles), then K and V tiles into a
 //              two-stage ring
 //   warp  9    TMEM allocator and MMA issuer (one thread)
+//   warp 10    gate: for every step j at which tile A has keys, waits
+//              for V(j) and K(j+1) to land, then arrives on tile A's P
+//              barrier, so the MMA thread waits twice per step (P_A with
+//              the loads, then P_B) instead of four times: each mbarrier
+//              wait on the issuing thread stalls the tensor pipe even when
+//              its phase has already completed.  The gate arrives for step
+//              j only after the phase of step j - 1 has completed, and the
+//              phase of step j completes only with tile A's P(j), whose S
+//              the MMA thread issued after passing step j - 1: the barrier
+//              stays within one phase of its waiters.  At the steps where
+//              tile A has no keys (the last step of a pair) the MMA thread
+//              waits for the loads itself.
 // TMEM (512 columns): per tile, S/P in 128 columns (P is written as packed
 // fp16 pairs over the first 64 columns of S) and O in head_dim columns.
 // The MMA thread ping-pongs: while softmax A works on S_A(j), the tensor core
@@ -77,10 +89,11 @@ using namespace ptx;
 
 constexpr int kBN = 128;            // keys per KV tile
 constexpr int kStages = 2;          // K/V ring depth
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kGateWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
@@ -197,7 +210,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         for (int t = 0; t < kNQ; ++t) {
             mbar_init(smem_u32(&bars.s_full[t]), 1);
-            mbar_init(smem_u32(&bars.p_full[t]), kBM);
+            mbar_init(smem_u32(&bars.p_full[t]), t == 0 ? kBM + 1 : kBM);  // tile A: + the gate
         }
         mbar_init(smem_u32(&bars.mma_done), 1);
         bars.abort = 0;
@@ -339,11 +352,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
             for (uint32_t j = 0; j < n_kv_all && ok; ++j) {
-                const uint32_t st = j % kStages, ph = (j / kStages) & 1;
-                ok = mbar_wait(smem_u32(&bars.v_full[st]), ph, wait_ns, status, kStatusTimeout);
-                if (!ok) break;
-                bool k_next_ready = false;
+                const uint32_t st = j % kStages;
                 const uint32_t jn = j + 1;
+                // Tile A's P barrier also carries the gate's word that V(j)
+                // and K(j+1) have landed; without tile A the loads are
+                // waited for here.
+                if (j >= tile_n[0]) {
+                    ok = mbar_wait(smem_u32(&bars.v_full[st]), (j / kStages) & 1, wait_ns, status,
+                                   kStatusTimeout);
+                    if (ok && jn < n_kv_all)
+                        ok = mbar_wait(smem_u32(&bars.k_full[jn % kStages]), (jn / kStages) & 1,
+                                       wait_ns, status, kStatusTimeout);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
                 for (int t = 0; t < kNQ && ok; ++t) {
                     if (j < tile_n[t]) {
                         ok = mbar_wait(smem_u32(&bars.p_full[t]), j & 1, wait_ns, status, kStatusTimeout);
@@ -351,25 +373,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         tc_fence_after();
                         issue_pv(t, j);
                     }
-                    if (jn < tile_n[t]) {
-                        if (!k_next_ready) {
-                            ok = mbar_wait(smem_u32(&bars.k_full[jn % kStages]),
-                                           (jn / kStages) & 1, wait_ns, status, kStatusTimeout);
-                            if (!ok) break;
-                            tc_fence_after();
-                            k_next_ready = true;
-                        }
-                        issue_s(t, jn);
-                    }
+                    if (jn < tile_n[t]) issue_s(t, jn);
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&bars.v_empty[st]));
-                if (k_next_ready) mma_commit(smem_u32(&bars.k_empty[jn % kStages]));
+                if (jn < n_kv_all) mma_commit(smem_u32(&bars.k_empty[jn % kStages]));
             }
             if (!ok) record_timeout(status, &bars);
             // Wait until every MMA this thread issued has completed.
             mma_commit(smem_u32(&bars.mma_done));
             mbar_wait(smem_u32(&bars.mma_done), 0, kDrainWaitNs);
+        }
+    } else if (warp == kGateWarp) {
+        // ------------------------------------------------------------ gate
+        if (lane == 0) {
+            bool ok = true;
+            for (uint32_t j = 0; j < tile_n[0] && ok; ++j) {
+                // the phase of step j - 1 completed: this arrival opens step j's
+                if (j > 0)
+                    ok = mbar_wait(smem_u32(&bars.p_full[0]), (j - 1) & 1, wait_ns, status,
+                                   kStatusTimeout);
+                if (ok)
+                    ok = mbar_wait(smem_u32(&bars.v_full[j % kStages]), (j / kStages) & 1, wait_ns,
+                                   status, kStatusTimeout);
+                if (ok && j + 1 < n_kv_all)
+                    ok = mbar_wait(smem_u32(&bars.k_full[(j + 1) % kStages]), ((j + 1) / kStages) & 1,
+                                   wait_ns, status, kStatusTimeout);
+                if (!ok) break;
+                mbar_arrive(smem_u32(&bars.p_full[0]));
+            }
+            if (!ok) record_timeout(status, &bars);
         }
     } else {
         // ------------------------------------------------------------ softmax
