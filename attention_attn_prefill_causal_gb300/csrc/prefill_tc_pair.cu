@@ -142,7 +142,7 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, TcBarriers*
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const __grid_constant__ CUtensorMap tm_po, uint32_t m,
                   uint32_t num_q_heads, uint32_t heads_per_kv,
@@ -656,7 +656,7 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     }
 
     {
-        const cudaError_t e = ensure_dynamic_smem<prefill_tc_kernel<D, BF16>>((int)L::kSmemAlloc);
+        const cudaError_t e = ensure_dynamic_smem<prefill_pair_kernel<D, BF16>>((int)L::kSmemAlloc);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchAttribute attr[1];
@@ -669,7 +669,7 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, BF16>, tq, tk, tv, to, tpo, m,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D, BF16>, tq, tk, tv, to, tpo, m,
                                        num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e,
                                        status, wait_ns, split);
     if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;

@@ -325,17 +325,28 @@ def remainder_graphs(bench, stream, append=True):
 TF32_PEAK_RATIO = 1.1 / 2.25
 
 
+def prefill_uses_pairs(m, num_q_heads, sms, tf32=False):
+    """The library's kernel choice: 16-bit calls whose query-tile pairs fill
+    the SMs twice over run the pair kernel (a work item is two 128-row query
+    tiles), the others and every TF32 call the single-tile kernel."""
+    return not tf32 and -(-m // 256) * num_q_heads >= 2 * sms
+
+
+def prefill_kernel(m, num_q_heads, sms, tf32=False):
+    """(name, source files) of the main kernel of a tensor-core prefill call."""
+    if prefill_uses_pairs(m, num_q_heads, sms, tf32):
+        return "prefill_pair_kernel", ["prefill_tc_pair.cu", "prefill_tc_common.cuh", "sm103_ptx.cuh"]
+    return "prefill_tc_kernel", ["prefill_tc.cu", "prefill_tc_common.cuh", "sm103_ptx.cuh"]
+
+
 def prefill_launches(m, num_q_heads, sms, tf32=False):
     """Kernels one tensor-core prefill call launches: the rounding pre-pass
     and the main kernel, plus the combine kernel when the call splits its key
-    walk.  Mirrors the library's plan: 16-bit calls whose query-tile pairs
-    fill the SMs twice over run the pair kernel (a work item is two 128-row
-    query tiles), the others and every TF32 call the single-tile kernel (one
-    tile); the key walk is split only when items x heads leave SMs idle, with
-    the smallest chunk whose items fit in one wave."""
+    walk.  Mirrors the library's plan: the key walk is split only when work
+    items x heads leave SMs idle, with the smallest chunk whose items fit in
+    one wave."""
     n_qt = -(-m // 128)
-    pairs = -(-m // 256)
-    tiles_per_item = 2 if (not tf32 and pairs * num_q_heads >= 2 * sms) else 1
+    tiles_per_item = 2 if prefill_uses_pairs(m, num_q_heads, sms, tf32) else 1
     n_units = -(-m // (128 * tiles_per_item))
 
     def nk(u):
@@ -446,7 +457,9 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
     tflops = flops / per_call / 1e12
     peak_key = "bf16_tflops_sustained" if secs > 1.0 else "bf16_tflops"
     peak = float(peaks[peak_key])
-    traffic = traffic_for(f"prefill_tc_kernel:{shape.name}", ["prefill_tc.cu", "sm103_ptx.cuh"])
+    kname, kfiles = prefill_kernel(shape.m, shape.num_q_heads,
+                                   torch.cuda.get_device_properties(device).multi_processor_count)
+    traffic = traffic_for(f"{kname}:{shape.name}", kfiles)
 
     # End to end through the Python API with page-locked host buffers: every
     # call's Q, K, V come from host memory (H2D copies) and its O goes back
@@ -540,7 +553,8 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
                "e2e": round(flops / e2e_per_call / 1e12, 2),
                "launches": pb.launches_per_call}
     detail = {"workload": shape.name, "calls": n, "flops_per_call": flops,
-              "peak": peak, "peak_source": f"{peak_key} ({peak_src})", "traffic": traffic,
+              "peak": peak, "peak_source": f"{peak_key} ({peak_src})", "kernel": kname,
+              "traffic": traffic,
               "l2": (f"inputs {pb.R} rotating replicas" if pb.R > 1 else "inputs larger than 2x L2"),
               "e2e_pipelined_ms": round(e2e_per_call * 1e3, 4),
               "e2e_serial_ms": round(serial_per_call * 1e3, 4),
