@@ -14,10 +14,10 @@
 // TMEM); P is rounded to nearest as the softmax packs it; fp16 inputs must
 // stay below 65504 (kStatusRange otherwise, after the fact).  TF32: a
 // kind::tf32 MMA uses the top 19 bits of each fp32 operand (the low 13
-// mantissa bits are dropped).  Q goes to the tensor core as the caller
-// stored it.  K and V are rounded to nearest TF32 by the pre-pass: an operand
-// dropped toward zero would bias the output (O = V[0] exactly for row 0),
-// which rounding to nearest halves and unbiases.  P is truncated to TF32 by
+// mantissa bits are dropped), so every operand is rounded to nearest TF32
+// first: Q by the softmax warps as they move it into TMEM, K and V by the
+// pre-pass.  An operand dropped toward zero would bias the output (O = V[0]
+// exactly for row 0), which rounding to nearest halves and unbiases.  P is truncated to TF32 by
 // the softmax itself and the row sum is taken over the truncated weights, so
 // the weights the MMA applies are normalised exactly (a row sum over the
 // untruncated weights would scale every output down by up to 2^-10 where the
@@ -446,6 +446,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         }
                         tmem_st16(lane_base + L::kQCol + c * 16, pk);
                     } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(round_tf32(__uint_as_float(r[i])));
                         tmem_st32(lane_base + L::kQCol + c * 32, r);
                     }
                 }

@@ -75,7 +75,7 @@ typedef enum {
     ATTN_PREC_BF16 = 2,
     /* Tensor-core mode with TF32 operands: tcgen05 kind::tf32 MMAs read fp32
      * data and use its top 19 bits (fp32's exponent, a 10-bit mantissa).  Q
-     * is used as stored; K and V are rounded to nearest TF32 by a pre-pass
+     * is rounded to nearest TF32 inside the kernel; K and V by a pre-pass
      * into the workspace (V also transposed); P is written as fp32; fp32
      * accumulation, softmax statistics and output.  No input range limit
      * beyond fp32's own; half the 16-bit tensor rate.  head_dim in {64, 128}. */
