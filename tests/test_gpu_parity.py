@@ -209,13 +209,29 @@ def test_decode_sharp_softmax(attn):
 @pytest.mark.parametrize("prec", [FP16, TF32])
 def test_prefill_split_into_many_key_chunks(attn, prec):
     """4096 tokens over 2 query heads leave most SMs idle, so the key walk of
-    each query-tile pair is split into chunks of four 128-key blocks: up to 8
-    chunk partials per row, more than one batch of the combine.  Sampled rows
-    include the first and last tiles."""
+    each query tile is split into chunks of 128-key blocks (nine blocks per
+    chunk on 152 SMs): up to 4 chunk partials per row, a full batch of the
+    combine.  Sampled rows include the first and last tiles."""
     m, hq, hkv, d = 4096, 2, 1, 64
     rows = workloads.sample_rows(m, 91)
     amax, _ = _check_prefill(attn, m, hq, hkv, d, prec, seed=91, rows=rows)
     print(f"split prefill m={m}: {len(rows)} rows, max abs {amax:.3e}")
+
+
+@pytest.mark.parametrize("side", [-1, 0])
+def test_prefill_fp16_kernel_choice_boundary(attn, side):
+    """16-bit calls whose query-tile pairs fill the SMs twice over run the
+    pair kernel, smaller ones the single-tile kernel.  16 heads and the
+    token count at which pairs x heads reaches 2 x SMs (side 0: the pair
+    kernel) or one pair less (side -1: the single-tile kernel), with sampled
+    rows checked against the oracle on both sides."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    hq, hkv, d = 16, 4, 128
+    pairs = -(-2 * sms // hq) + side
+    m = 256 * pairs
+    rows = workloads.sample_rows(m, 93 + side, 24, 24, 48)
+    amax, _ = _check_prefill(attn, m, hq, hkv, d, FP16, seed=93 + side, rows=rows)
+    print(f"fp16 m={m} ({pairs} pairs x {hq} heads, {sms} SMs): {len(rows)} rows, max abs {amax:.3e}")
 
 
 @pytest.mark.parametrize("prec", [FP16, TF32, FP32])
