@@ -101,6 +101,8 @@ cudaError_t launch_prefill_fp32(const float* q, const float* k, const float* v, 
                                 uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,
                                 float scale, cudaStream_t stream);
 
+// 16-bit tensor-core prefill (prefill_tc.cu): the single-tile kernel, or the
+// pair kernel below for grids of at least two waves of query-tile pairs.
 size_t prefill_tc_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                   uint32_t head_dim);
 
@@ -125,7 +127,8 @@ cudaError_t launch_prefill_pair(const float* q, const float* k, const float* v, 
 size_t prefill_tf32_workspace_bytes(uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                     uint32_t head_dim);
 
-// TF32 tensor-core prefill; cudaErrorNotSupported as launch_prefill_tc.
+// TF32 tensor-core prefill (the single-tile kernel in prefill_tc.cu);
+// cudaErrorNotSupported as launch_prefill_tc.
 cudaError_t launch_prefill_tf32(const float* q, const float* k, const float* v, float* o,
                                 uint32_t m, uint32_t num_q_heads, uint32_t num_kv_heads,
                                 uint32_t head_dim, uint32_t q_stride, uint32_t kv_stride,

@@ -62,6 +62,9 @@
 // Every mbarrier wait is bounded; on a timeout a thread records
 // kStatusTimeout, abandons its loop, and the CTA still drains its copies,
 // waits for its MMAs and frees TMEM before exiting.
+// 16-bit grids of at least two waves of query-tile pairs run the pair kernel
+// of prefill_tc_pair.cu instead (prefill_use_pairs below), whose loads and
+// hand-offs each serve twice the MMAs; TF32 calls always run this kernel.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

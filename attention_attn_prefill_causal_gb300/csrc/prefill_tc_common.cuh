@@ -1,8 +1,8 @@
 // prefill_tc_common.cuh -- pieces shared by the two tensor-core prefill
-// kernels (16-bit operands in prefill_tc.cu, TF32 operands in
-// prefill_tf32.cu): the split of small problems' key walks into chunks, the
-// combine kernel that merges the chunks' partial results, and the TMA tensor
-// map encoding.
+// kernels (the single-tile kernel in prefill_tc.cu, the query-tile-pair
+// kernel in prefill_tc_pair.cu): the split of small problems' key walks into
+// chunks, the combine kernel that merges the chunks' partial results, the
+// 16-bit rounding pre-pass and the TMA tensor map encoding.
 //
 // Operation ("aprender-gpu 0.32.0 -- prefill_fused.rs", module doc,
 // Algorithm 1-3): causal grouped-query attention with an online softmax.  A
@@ -37,9 +37,10 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Split-KV scheduling for small grids: a query-tile pair's keys are walked in
-// chunks of kv_chunk tiles by separate CTAs; split pairs leave per-chunk
-// partials that prefill_combine_kernel merges.  kv_chunk = ~0u: no split.
+// Split-KV scheduling for small grids: a work item's keys (one query tile,
+// or a pair of them) are walked in chunks of kv_chunk tiles by separate CTAs;
+// split items leave per-chunk partials that prefill_combine_kernel merges.
+// kv_chunk = ~0u: no split.
 // Chunks always cover whole 128-key blocks (kv_chunk is a multiple of
 // kv_per_qtile), so every chunk that reaches a query tile's diagonal block
 // holds a key for each of its rows.
