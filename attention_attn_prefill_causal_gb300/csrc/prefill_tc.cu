@@ -395,6 +395,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // load order; S(0) and S(1) took the first ones.  go(j) reuses the
         // barrier of step j - 2, whose phase must complete first (its P
         // arrivals precede this step's, so none can land in the old phase).
+        // A slot's parity wait is exact only once the slot's previous load
+        // has landed: the gate checks every load after those of S(0) and
+        // S(1) itself, and first waits for S(0) and S(1) to complete, which
+        // the MMA thread issued only after their loads had landed (with two
+        // pieces per tile, K(2)'s second piece reuses the slot of K(0)'s
+        // first, and a wait for it could otherwise pass on the earlier phase).
         if (lane == 0) {
             uint32_t load = (uint32_t)L::kPieces * min(nkv, 2u);
             bool ok = true;
@@ -402,6 +408,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (j >= 2)
                     ok = mbar_wait(smem_u32(&bars.go[j & 1u]), ((j - 2) >> 1) & 1, wait_ns, status,
                                    kStatusTimeout);
+                else
+                    ok = mbar_wait(smem_u32(&bars.s_full[j]), 0, wait_ns, status, kStatusTimeout);
                 const uint32_t n = (uint32_t)L::kPieces * (j + 2 < nkv ? 2u : 1u);
                 for (uint32_t i = 0; i < n && ok; ++i, ++load)
                     ok = mbar_wait(smem_u32(&bars.full[load % kSlots]), (load / kSlots) & 1, wait_ns,
