@@ -41,7 +41,9 @@
 // MMAs consume them: K(0), K(1), V(0), K(2), V(1), K(3), ...  The MMA thread
 // issues S(0), S(1), then per step j: P(j).V, then S(j+2) into the buffer
 // P(j) occupied (MMAs execute in issue order, so S(j+2) overwrites P(j)
-// after P(j).V has read it).  A slot is released by a commit right after the
+// after P(j).V has read it).  With one piece per tile a slot is reused once
+// the S that follows its tile's MMAs has completed (every tcgen05.commit
+// between MMAs costs the tensor pipe); with two, by a commit right after the
 // MMAs that read it.
 // Warp roles (224 threads): warps 0-3 softmax (thread = TMEM lane = query
 // row), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer, warp 6
@@ -127,14 +129,19 @@ struct TcLayout {
     static_assert(kVBoxesPerPiece * kVBoxBytes == kPieceBytes, "V piece");
     static_assert(kQSlots * kSlotBytes == kQ32Bytes, "query staging");
     static_assert(kSmemAlloc <= 227 * 1024, "shared memory");
+    // One piece per tile: the ring holds seven tiles, so a slot can wait to
+    // be released by the completion of the next S (no release commits).  Two
+    // pieces per tile (TF32 at D = 128) leave 3.5 tiles, and a slot must be
+    // released as soon as its own MMAs complete.
+    static constexpr bool kReleaseByS = kPieces == 1;
 };
 
 struct __align__(8) TcBarriers {
     uint64_t q_full;        // the fp32 query tile landed in the staging slots
     uint64_t q_ready;       // the query tile is in TMEM (every softmax thread arrives)
     uint64_t full[kSlots];
-    uint64_t empty[kSlots];
-    uint64_t s_full[2];     // S(j) in buffer j % 2 computed
+    uint64_t empty[kSlots];  // slot's MMAs completed (two-piece tiles only)
+    uint64_t s_full[4];      // S(j) computed, by step j % 4 (its buffer is j % 2)
     uint64_t go[2];         // step j % 2: P(j) written and the slots of V(j), K(j+2) loaded
     uint64_t pv_last;       // P.V of the second-to-last step completed (one phase)
     uint64_t mma_done;
@@ -209,10 +216,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_init(smem_u32(&bars.full[s]), 1);
             mbar_init(smem_u32(&bars.empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&bars.s_full[b]), 1);
-            mbar_init(smem_u32(&bars.go[b]), kSoftmaxThreads + 1);
-        }
+        for (int b = 0; b < 4; ++b) mbar_init(smem_u32(&bars.s_full[b]), 1);
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&bars.go[b]), kSoftmaxThreads + 1);
         mbar_init(smem_u32(&bars.pv_last), 1);
         mbar_init(smem_u32(&bars.mma_done), 1);
         bars.abort = 0;
@@ -270,7 +275,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             bool ok = true;
             for (uint32_t n = 0; n < n_loads; ++n) {
                 const uint32_t slot = n % kSlots, use = n / kSlots;
-                if (use > 0) {
+                if (use > 0 && L::kReleaseByS) {
+                    // The slot's previous tile has been read once S(x)
+                    // completed: S(i) for K(i), and for V(i) the S(i + 2)
+                    // issued right after P(i).V (a V tile with no later S is
+                    // among the last loads, whose slots are never reused).
+                    // The witnesses never decrease, and S(x + 4) needs
+                    // K(x + 4), not issued yet: each parity wait is exact.
+                    bool was_k;
+                    uint32_t was_step;
+                    unit_of((n - kSlots) / L::kPieces, was_k, was_step);
+                    const uint32_t x = was_k ? was_step : was_step + 2;
+                    ok = mbar_wait(smem_u32(&bars.s_full[x & 3u]), (x >> 2) & 1, wait_ns, status,
+                                   kStatusTimeout);
+                } else if (use > 0) {
                     ok = mbar_wait(smem_u32(&bars.empty[slot]), (use - 1) & 1, wait_ns, status,
                                    kStatusTimeout);
                 } else if (slot >= (uint32_t)L::kQStageSlot) {
@@ -349,9 +367,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                    b0 + (uint64_t)((ks / 4) * (kBoxBytes / 16) + (ks % 4) * 2),
                                    idesc_s, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(smem_u32(&bars.empty[slot]));
+                    if (!L::kReleaseByS) mma_commit(smem_u32(&bars.empty[slot]));
                 }
-                mma_commit(smem_u32(&bars.s_full[j & 1u]));
+                mma_commit(smem_u32(&bars.s_full[j & 3u]));
                 return true;
             };
             auto issue_pv = [&](uint32_t j) {
@@ -368,7 +386,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                 : (uint64_t)((ks / 4) * (L::kVBoxBytes / 16) + (ks % 4) * 2);
                         mma_ts<OP>(d, a + k * 8, b0 + boff, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(smem_u32(&bars.empty[slot]));
+                    if (!L::kReleaseByS) mma_commit(smem_u32(&bars.empty[slot]));
                 }
                 // The last step's softmax rescales O only after this group
                 // (S(j+2), whose completion tells the other steps, does not exist).
@@ -476,7 +494,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         float l_sum = 0.f;
         for (uint32_t j = 0; j < nkv && ok; ++j) {
             const uint32_t buf = j & 1u;
-            ok = mbar_wait(smem_u32(&bars.s_full[buf]), (j >> 1) & 1, wait_ns, status, kStatusTimeout);
+            ok = mbar_wait(smem_u32(&bars.s_full[j & 3u]), (j >> 2) & 1, wait_ns, status,
+                           kStatusTimeout);
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             tc_fence_after();
             const uint32_t t_s = lane_base + buf * kBK;
@@ -559,7 +578,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 // S(j+1) was issued right after it, and the last step has its
                 // own barrier.  (Waiting on S(j+1) here consumes the same phase
                 // the next step waits for.)
-                ok = j + 1 < nkv ? mbar_wait(smem_u32(&bars.s_full[buf ^ 1u]), ((j + 1) >> 1) & 1,
+                ok = j + 1 < nkv ? mbar_wait(smem_u32(&bars.s_full[(j + 1) & 3u]), ((j + 1) >> 2) & 1,
                                              wait_ns, status, kStatusTimeout)
                                  : mbar_wait(smem_u32(&bars.pv_last), 0, wait_ns, status,
                                              kStatusTimeout);
