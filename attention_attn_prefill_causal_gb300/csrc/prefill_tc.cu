@@ -55,8 +55,9 @@
 // The softmax rescales O only when the running max grows by more than 8
 // (log2 units); it then first waits for the previous P.V (O stable).
 // Epilogue: O (normalised, or a chunk's unnormalised partial) into the ring's
-// first slots, then TMA stores of whole 128-byte lines.  Small grids split
-// each tile's key walk into chunks merged by the combine kernel.
+// first slots, then each warp writes its 32 rows back with whole-line
+// stores.  Small grids split each tile's key walk into chunks merged by the
+// combine kernel.
 // Launch chain (programmatic dependent launches): the pre-pass waits for the
 // kernel before the call, then lets this kernel launch; this kernel stages
 // the caller's Q at once and waits for the pre-pass before its first K/V
@@ -166,9 +167,8 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
 template <int D, Op OP>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const __grid_constant__ CUtensorMap tm_po, uint32_t m,
-                  uint32_t num_q_heads, uint32_t heads_per_kv,
+                  const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, uint32_t o_stride,
+                  uint32_t m, uint32_t num_q_heads, uint32_t heads_per_kv,
                   float scale_log2, unsigned int* status, uint64_t wait_ns,
                   const SplitArgs split) {
     using L = TcLayout<D, OP>;
@@ -599,7 +599,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mbar_arrive(smem_u32(&bars.go[buf]));
         }
         // ---- epilogue: O (normalised, or this chunk's unnormalised partial)
-        // into the ring's first slots, then TMA stores of whole lines.
+        // into the ring's first slots; each warp then writes the 32 rows it
+        // staged back with whole-line stores.
         const bool split_item = n_chunks > 1;
         if (ok && nkv > 0) {
             ok = mbar_wait(smem_u32(&bars.mma_done), 0, wait_ns, status, kStatusTimeout);
@@ -628,22 +629,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 const size_t pidx = ((size_t)chunk * num_q_heads + h) * split.m_pad + row;
                 *reinterpret_cast<float2*>(split.part_ml + 2 * pidx) = make_float2(m_used, l_sum);
             }
-            fence_proxy_async_smem();
-        }
-        named_barrier(1, kSoftmaxThreads);
-        if (ok && nkv > 0 && warp == 0 && lane == 0) {
-            const int32_t y0 = (int32_t)tile_row0;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                const uint32_t src = smem_u32(stage + c * kBoxBytes);
-                if (split_item)
-                    tma_store_2d(&tm_po, src, c * 32,
-                                 (int32_t)((chunk * num_q_heads + h) * split.m_pad) + y0);
-                else
-                    tma_store_2d(&tm_o, src, (int32_t)(h * D + c * 32), y0);
-            }
-            bulk_commit_group();
-            bulk_wait_all_read();  // the staging must outlive the reads, not the writes
+            __syncwarp();
+            float* dst = split_item
+                             ? split.part_o + ((size_t)(chunk * num_q_heads + h) * split.m_pad + tile_row0) * D
+                             : o + (size_t)tile_row0 * o_stride + h * D;
+            store_warp_rows<D>(stage, kBoxBytes, (uint32_t)warp * 32, min(m - tile_row0, (uint32_t)kBM),
+                               dst, split_item ? (size_t)D : (size_t)o_stride, lane);
         }
         if (!ok && lane == 0) record_timeout(status, &bars);
     }
@@ -772,9 +763,8 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
                                    kv_cols, kv_stride, status);
         if (e != cudaSuccess) return e;
     }
-    CUtensorMap tq, tk, tv, to, tpo;
-    bool maps = encode_output_map(&tq, q, q_cols, m, q_stride, kBM) &&
-                encode_output_map(&to, o, q_cols, m, q_stride, kBM);
+    CUtensorMap tq, tk, tv;
+    bool maps = encode_output_map(&tq, q, q_cols, m, q_stride, kBM);
     if constexpr (kTf32)
         maps = maps && encode_output_map(&tk, kw, kv_cols, m, kv_cols, kBK) &&
                encode_output_map(&tv, vw, m, kv_cols, w.m4, D);
@@ -782,13 +772,6 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
         maps = maps && encode_operand_map(&tk, kw, kv_cols, m, kBK, OP == Op::BF16) &&
                encode_operand_map(&tv, vw, kv_cols, m, kBK, OP == Op::BF16);
     if (!maps) return cudaErrorNotSupported;
-    if (split.kv_chunk != kNoSplit) {
-        if (!encode_output_map(&tpo, split.part_o, D,
-                               (uint64_t)split.n_chunks_max * num_q_heads * split.m_pad, D, kBM))
-            return cudaErrorNotSupported;
-    } else {
-        tpo = to;  // not used without a split
-    }
     {
         const cudaError_t e = ensure_dynamic_smem<prefill_tc_kernel<D, OP>>((int)L::kSmemAlloc);
         if (e != cudaSuccess) return e;
@@ -800,7 +783,7 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, OP>, tq, tk, tv, to, tpo, m,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D, OP>, tq, tk, tv, o, q_stride, m,
                                        num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e,
                                        status, wait_ns, split);
     if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;

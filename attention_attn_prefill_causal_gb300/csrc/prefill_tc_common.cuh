@@ -62,6 +62,32 @@ __device__ __forceinline__ uint32_t kv_tiles_for(uint32_t qt, uint32_t m, uint32
     return (qt * kBM < m) ? (qt + 1) * per : 0;
 }
 
+// Output write-back.  An fp32 tile of O is staged as D/32 boxes of 128 rows
+// x 128 bytes, box b holding columns [32b, 32b + 32) with the 16-byte chunks
+// of row r XOR-swizzled by r % 8.  One warp writes rows [row0, row0 + 32) of
+// it to dst (row r at dst + r * pitch floats) with whole-line stores: a store
+// instruction covers one row at D = 128 (32 lanes x 16 bytes) and two rows at
+// D = 64.  Rows at or past `rows` are not written.  (A TMA store of the same
+// tile took about 1 us per CTA to read its 64 KB of shared memory.)
+template <int D>
+__device__ __forceinline__ void store_warp_rows(const uint8_t* stage, uint32_t box_bytes,
+                                                uint32_t row0, uint32_t rows, float* dst,
+                                                size_t pitch, uint32_t lane) {
+    constexpr uint32_t kChunks = D / 4;              // 16-byte chunks per row
+    constexpr uint32_t kRowsPerStore = 32 / kChunks;
+    const uint32_t sub = lane / kChunks, chunk = lane % kChunks;
+    const uint32_t box = chunk / 8, c8 = chunk % 8;
+#pragma unroll 8
+    for (uint32_t i = 0; i < 32; i += kRowsPerStore) {
+        const uint32_t r = row0 + i + sub;
+        if (r < rows) {
+            const float4 v = *reinterpret_cast<const float4*>(stage + box * box_bytes + r * 128 +
+                                                              ((c8 ^ (r & 7u)) * 16));
+            *reinterpret_cast<float4*>(dst + (size_t)r * pitch + chunk * 4) = v;
+        }
+    }
+}
+
 // Merge of the KV-chunk partials of split query-tile pairs.  A thread owns 8
 // consecutive elements of one (row, head); the 16 (D = 128) threads of a row
 // read and write whole 512-byte rows.  Up to kCombineBatch chunks are merged

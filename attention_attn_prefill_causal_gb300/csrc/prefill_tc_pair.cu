@@ -56,8 +56,9 @@
 // is exact either way, and P stays below 2^8.
 // Epilogue: after the CTA's last MMA the K/V ring is free; each softmax
 // thread writes its row of O into 128-byte swizzled staging boxes there, and
-// one thread per tile stores them with TMA tensor stores, so O leaves in
-// whole 128-byte lines rather than one 16-byte piece per row and instruction.
+// each warp then writes the 32 rows it staged back, a whole row (or two at
+// D = 64) per store instruction, so O leaves in whole 128-byte lines rather
+// than one 16-byte piece per row and instruction.
 // Small grids (query-tile pairs x heads below the SM count) split each
 // pair's key walk into chunks of C tiles, one work item per chunk; chunks
 // write unnormalised partials and a combine kernel merges them.
@@ -107,7 +108,7 @@ struct TcLayout {
     static constexpr uint32_t kBytes = kVOff + kStages * kKTileBytes;
     static constexpr uint32_t kSmemAlloc = kBytes + 1024;        // room to align to 1 KB
     // Epilogue: once every MMA has completed, the K/V ring stages the fp32
-    // output tiles for the TMA stores, as D/32 boxes of 128 rows x 128 bytes
+    // output tiles for the write-back, as D/32 boxes of 128 rows x 128 bytes
     // (32 floats) in the 128-byte swizzled layout.
     static constexpr uint32_t kOBoxBytes = kBM * 128;
     static constexpr uint32_t kOTileBytes = kBM * D * 4;
@@ -143,9 +144,8 @@ __device__ __forceinline__ void record_timeout(unsigned int* status, TcBarriers*
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const __grid_constant__ CUtensorMap tm_po, uint32_t m,
-                  uint32_t num_q_heads, uint32_t heads_per_kv,
+                  const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, uint32_t o_stride,
+                  uint32_t m, uint32_t num_q_heads, uint32_t heads_per_kv,
                   float scale_log2, unsigned int* status, uint64_t wait_ns,
                   const SplitArgs split) {
     using L = TcLayout<D>;
@@ -535,9 +535,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         // ---- epilogue.  After the CTA's last MMA the K/V ring is free: each
         // thread writes its row of O (normalised, or this chunk's unnormalised
-        // partial) into the swizzled staging boxes, and one thread of the
-        // warpgroup stores the tile with TMA (whole 128-byte lines; rows past
-        // m are clipped by the tensor map).
+        // partial) into the swizzled staging boxes, and each warp then writes
+        // the 32 rows it staged back with whole-line stores (rows past m are
+        // not written).
         const bool split_item = n_chunks > 1;
         if (ok && nkv > 0) {
             ok = mbar_wait(smem_u32(&bars.mma_done), 0, wait_ns, status, kStatusTimeout);
@@ -575,22 +575,13 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const size_t pidx = ((size_t)chunk * num_q_heads + h) * split.m_pad + row;
                 *reinterpret_cast<float2*>(split.part_ml + 2 * pidx) = make_float2(m_used, l_sum);
             }
-            fence_proxy_async_smem();
-        }
-        named_barrier(1 + t, 128);
-        if (ok && nkv > 0 && wq == 0 && lane == 0) {
-            const int32_t y0 = (int32_t)((qt0 + t) * kBM);
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                const uint32_t src = smem_u32(stage + c * L::kOBoxBytes);
-                if (split_item)
-                    tma_store_2d(&tm_po, src, c * 32,
-                                 (int32_t)((chunk * num_q_heads + h) * split.m_pad) + y0);
-                else
-                    tma_store_2d(&tm_o, src, (int32_t)(h * D + c * 32), y0);
-            }
-            bulk_commit_group();
-            bulk_wait_all_read();  // the staging must outlive the reads, not the writes
+            __syncwarp();
+            const uint32_t tile_row0 = (qt0 + t) * kBM;
+            float* dst = split_item
+                             ? split.part_o + ((size_t)(chunk * num_q_heads + h) * split.m_pad + tile_row0) * D
+                             : o + (size_t)tile_row0 * o_stride + h * D;
+            store_warp_rows<D>(stage, L::kOBoxBytes, (uint32_t)wq * 32, min(m - tile_row0, (uint32_t)kBM),
+                               dst, split_item ? (size_t)D : (size_t)o_stride, lane);
         }
         if (!ok && lane == 0) record_timeout(status, &bars);
     }
@@ -641,19 +632,11 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
                                            kv_cols, kv_stride, status);
         if (e != cudaSuccess) return e;
     }
-    CUtensorMap tq, tk, tv, to, tpo;
+    CUtensorMap tq, tk, tv;
     if (!encode_output_map(&tq, q, q_cols, m, q_stride, kBM) ||
         !encode_operand_map(&tk, kh, kv_cols, m, kBN, BF16) ||
-        !encode_operand_map(&tv, vh, kv_cols, m, kBN, BF16) ||
-        !encode_output_map(&to, o, q_cols, m, q_stride, kBM))
+        !encode_operand_map(&tv, vh, kv_cols, m, kBN, BF16))
         return cudaErrorNotSupported;
-    if (split.kv_chunk != kNoSplit) {
-        if (!encode_output_map(&tpo, split.part_o, D,
-                               (uint64_t)split.n_chunks_max * num_q_heads * split.m_pad, D, kBM))
-            return cudaErrorNotSupported;
-    } else {
-        tpo = to;  // not used without a split
-    }
 
     {
         const cudaError_t e = ensure_dynamic_smem<prefill_pair_kernel<D, BF16>>((int)L::kSmemAlloc);
@@ -669,7 +652,7 @@ cudaError_t launch_tc(const float* q, const float* k, const float* v, float* o, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D, BF16>, tq, tk, tv, to, tpo, m,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D, BF16>, tq, tk, tv, o, q_stride, m,
                                        num_q_heads, num_q_heads / num_kv_heads, scale * kLog2e,
                                        status, wait_ns, split);
     if (e != cudaSuccess || split.kv_chunk == kNoSplit) return e;

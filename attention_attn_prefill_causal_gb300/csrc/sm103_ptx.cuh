@@ -79,36 +79,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         ::"r"(dst), "l"(tmap), "r"(bar), "r"(x), "r"(y) : "memory");
 }
 
-// 2-D tiled tensor store shared -> global (bulk async group).  Rows or
-// columns of the box outside the tensor's extent are not written.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x,
-                                             int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
-        ::"l"(tmap), "r"(src), "r"(x), "r"(y) : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until every committed bulk group of this thread has finished reading
-// its shared-memory source (the global writes may still be in flight; they
-// complete before the grid does).
-__device__ __forceinline__ void bulk_wait_all_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Barrier over `count` threads (a multiple of 32) on hardware barrier `id`.
-// Every lane of each participating warp calls it; the warp reconverges
-// first (bar.sync is warp-aligned).
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-    __syncwarp();
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
