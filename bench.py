@@ -197,6 +197,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
+def lead_in():
+    """Keep the GPU busy for about half a millisecond on the current stream
+    before a device-timed region starts.  Without it the start event runs
+    on an idle GPU at once and the region then waits for the host to submit
+    its first graph launch, a fixed cost that short runs spread over few
+    steps (about 35 us at 20 steps).  The spin runs before the start event,
+    so the region still holds exactly the timed steps."""
+    torch.cuda._sleep(1_000_000)  # clock cycles: about 0.5 ms at 2 GHz
+
+
 def make_graph(fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -290,6 +300,7 @@ def time_steps(graph, R, rem_graphs, steps, stream):
         torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        lead_in()
         start.record(stream)
         run_graph_steps(graph, R, rem_graphs, steps)
         end.record(stream)
@@ -425,6 +436,7 @@ def time_prefill_calls(pb, stream, calls):
     reps = max(1, math.ceil(calls / pb.R))
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        lead_in()
         start.record(stream)
         for _ in range(reps):
             g.replay()
@@ -586,6 +598,7 @@ def copy_floor_us(replicas, traffic_bytes, stream, reps=50):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        lead_in()
         e0.record(stream)
         for _ in range(reps):
             g.replay()
@@ -661,6 +674,7 @@ def bench_prefill_fp32_small(attn, shape, device, stream, calls, peaks):
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        lead_in()
         e0.record(stream)
         for _ in range(reps):
             g.replay()
@@ -703,6 +717,8 @@ def bench_layer_stack(attn, shape, device, stream, layers=28, reps=5):
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            lead_in()
         t0 = time.perf_counter()
         with torch.cuda.stream(stream):
             e0.record(stream)
