@@ -68,7 +68,8 @@ __device__ __forceinline__ uint32_t kv_tiles_for(uint32_t qt, uint32_t m, uint32
 // it to dst (row r at dst + r * pitch floats) with whole-line stores: a store
 // instruction covers one row at D = 128 (32 lanes x 16 bytes) and two rows at
 // D = 64.  Rows at or past `rows` are not written.  (A TMA store of the same
-// tile took about 1 us per CTA to read its 64 KB of shared memory.)
+// tile moves it out at the same rate, about 64 KB per us per SM; these stores
+// need no tensor map, and the CTA need not wait for a bulk store's reads.)
 template <int D>
 __device__ __forceinline__ void store_warp_rows(const uint8_t* stage, uint32_t box_bytes,
                                                 uint32_t row0, uint32_t rows, float* dst,
