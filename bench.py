@@ -628,6 +628,9 @@ def bench_decode_companion(attn, shape, device, stream, steps, peaks, peak_src):
                "frac": round(gbs / hbm, 4), "err": float(f"{err:.3g}")}
     if shape.window:
         compact["copy_floor_us"] = round(copy_floor_us(db.kc, live, stream), 3)
+        # the same time over the formula's byte count (all total_seq rows,
+        # which the kernel does not read: rows below the window are skipped)
+        compact["gbs_all_rows_formula"] = round(shape.kv_bytes_all_rows() / per / 1e9, 2)
     detail = {"workload": shape.name, "steps": n, "bytes_per_step": live,
               "bytes_all_rows": shape.kv_bytes_all_rows(),
               "gbs_all_rows_formula": round(shape.kv_bytes_all_rows() / per / 1e9, 2),
