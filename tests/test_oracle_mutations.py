@@ -43,6 +43,20 @@ MUTANTS = {
     "rope_query_not_rotated": ("if (rope_cos) rope(tmp, rope_cos, rope_sin, d, qd + (size_t)h * d);",
                                "if (0) rope(tmp, rope_cos, rope_sin, d, qd + (size_t)h * d);"),
     "fused_value_not_appended": ("v_cache[dst] = v_new[(size_t)g * d + e];", "(void)dst;"),
+    # Each mutant below stays inside the buffers it reads (the pins run it
+    # in this process).
+    "causal_mask_dropped": ("if (j > i) { s[j] = -INFINITY; continue; }", ""),
+    "value_gqa_interleaved": ("softmax_weighted_sum(s, m, v + (size_t)kvh * d, kv_stride, d, out);",
+                              "softmax_weighted_sum(s, m, v + (size_t)(h % num_kv_heads) * d, kv_stride, d, out);"),
+    "query_head_is_kv_head": ("const float *qi = q + (size_t)i * q_stride + (size_t)h * d;",
+                              "const float *qi = q + (size_t)i * q_stride + (size_t)kvh * d;"),
+    "decode_newest_row_dropped": ("softmax_weighted_sum(s, total_seq, vb, d, d, out + (size_t)h * d);",
+                                  "softmax_weighted_sum(s, total_seq - 1, vb, d, d, out + (size_t)h * d);"),
+    "window_mask_minus_infinity": ("if (t < ws) s[t] = -1.0e4;", "if (t < ws) s[t] = -INFINITY;"),
+    "cache_head_pitch_total_seq": ("const float *kb = k_cache + (size_t)kvh * max_seq * d;",
+                                   "const float *kb = k_cache + (size_t)kvh * total_seq * d;"),
+    "rope_cos_sin_swapped": ("const double c = (double)cosv[i], sn = (double)sinv[i];",
+                             "const double c = (double)sinv[i], sn = (double)cosv[i];"),
 }
 
 
