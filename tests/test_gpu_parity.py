@@ -790,6 +790,23 @@ def test_prefill_bf16_operands(attn, m, hq, hkv, d):
     assert compare(got16, ref)[0] <= TC_ABS
 
 
+def test_prefill_bf16_operands_pair_kernel(attn):
+    """The bf16 mode through the query-tile-pair kernel: 16 pairs x 40 heads
+    fill two waves of SMs.  Sampled rows against the oracle at the bf16 bound
+    (reading 16), and the fp16 mode at 3e-3 on the same inputs."""
+    m, hq, hkv, d = 4096, 40, 8, 128
+    assert (m // 256) * hq >= 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    qs, kvs = hq * d, hkv * d
+    q, k, v = workloads.prefill_inputs(m, qs, kvs, seed=77)
+    rows = workloads.sample_rows(m, 77, 32, 32, 64)
+    ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), m, hq, hkv, d, qs, kvs, rows=rows)
+    got = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, BF16)[rows]
+    amax, _ = compare(got, ref)
+    assert amax <= 2.5e-2, amax
+    got16 = _run_prefill(attn, q, k, v, m, hq, hkv, d, qs, kvs, FP16)[rows]
+    assert compare(got16, ref)[0] <= TC_ABS
+
+
 # ------------------------------------------------------------------ TF32 operand mode
 
 @pytest.mark.parametrize("d", [64, 128])
