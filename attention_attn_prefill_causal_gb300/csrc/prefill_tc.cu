@@ -43,8 +43,8 @@
 // P(j) occupied (MMAs execute in issue order, so S(j+2) overwrites P(j)
 // after P(j).V has read it).  With one piece per tile a slot is reused once
 // the S that follows its tile's MMAs has completed (every tcgen05.commit
-// between MMAs costs the tensor pipe); with two, by a commit right after the
-// MMAs that read it.
+// between MMAs costs the tensor pipe); with two, a K slot once its own S has
+// completed, a V slot by a commit right after the P.V MMAs that read it.
 // Warp roles (224 threads): warps 0-3 softmax (thread = TMEM lane = query
 // row), warp 4 TMA producer, warp 5 TMEM allocator and MMA issuer, warp 6
 // gate.  An mbarrier wait on the issuing thread stalls the tensor pipe even
@@ -133,7 +133,8 @@ struct TcLayout {
     // One piece per tile: the ring holds seven tiles, so a slot can wait to
     // be released by the completion of the next S (no release commits).  Two
     // pieces per tile (TF32 at D = 128) leave 3.5 tiles, and a slot must be
-    // released as soon as its own MMAs complete.
+    // released as soon as its own MMAs complete: a K slot by its S's
+    // completion, a V slot by a commit after its P.V.
     static constexpr bool kReleaseByS = kPieces == 1;
 };
 
@@ -141,7 +142,7 @@ struct __align__(8) TcBarriers {
     uint64_t q_full;        // the fp32 query tile landed in the staging slots
     uint64_t q_ready;       // the query tile is in TMEM (every softmax thread arrives)
     uint64_t full[kSlots];
-    uint64_t empty[kSlots];  // slot's MMAs completed (two-piece tiles only)
+    uint64_t empty[kSlots];  // a V piece's P.V completed (two-piece tiles only)
     uint64_t s_full[4];      // S(j) computed, by step j % 4 (its buffer is j % 2)
     uint64_t go[2];         // step j % 2: P(j) written and the slots of V(j), K(j+2) loaded
     uint64_t pv_last;       // P.V of the second-to-last step completed (one phase)
@@ -272,10 +273,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             asm volatile("griddepcontrol.wait;" ::: "memory");
             const uint32_t n_loads = n_units * L::kPieces;
             uint32_t issued = 0;
+            // Two-piece tiles: per slot, the parity of the V pieces loaded
+            // into it so far (its release barrier completes once per V piece).
+            uint32_t v_parity = 0;
             bool ok = true;
             for (uint32_t n = 0; n < n_loads; ++n) {
                 const uint32_t slot = n % kSlots, use = n / kSlots;
-                if (use > 0 && L::kReleaseByS) {
+                bool prev_k = false;
+                uint32_t prev_step = 0;
+                if (use > 0) unit_of((n - kSlots) / L::kPieces, prev_k, prev_step);
+                if (use > 0 && !L::kReleaseByS && prev_k) {
+                    // A K tile's slots are free once its S has completed
+                    // (S(x + 4) needs K(x + 4), not issued yet: the wait is
+                    // exact).
+                    ok = mbar_wait(smem_u32(&bars.s_full[prev_step & 3u]), (prev_step >> 2) & 1,
+                                   wait_ns, status, kStatusTimeout);
+                } else if (use > 0 && L::kReleaseByS) {
                     // The slot's previous tile has been read once S(x)
                     // completed: S(i) for K(i), and for V(i) the S(i + 2)
                     // issued right after P(i).V (a V tile with no later S is
@@ -289,8 +302,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ok = mbar_wait(smem_u32(&bars.s_full[x & 3u]), (x >> 2) & 1, wait_ns, status,
                                    kStatusTimeout);
                 } else if (use > 0) {
-                    ok = mbar_wait(smem_u32(&bars.empty[slot]), (use - 1) & 1, wait_ns, status,
-                                   kStatusTimeout);
+                    // a V piece: released by the commit after its P.V MMAs
+                    ok = mbar_wait(smem_u32(&bars.empty[slot]), ((v_parity >> slot) & 1u) ^ 1u,
+                                   wait_ns, status, kStatusTimeout);
                 } else if (slot >= (uint32_t)L::kQStageSlot) {
                     // the query staging slots are free once the tile is in TMEM
                     ok = mbar_wait(smem_u32(&bars.q_ready), 0, wait_ns, status, kStatusTimeout);
@@ -299,6 +313,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 bool is_k;
                 uint32_t step;
                 unit_of(n / L::kPieces, is_k, step);
+                if (!is_k) v_parity ^= 1u << slot;
                 const uint32_t piece = n % L::kPieces;
                 const uint32_t bar = smem_u32(&bars.full[slot]);
                 const uint32_t dst = sR + slot * kSlotBytes;
@@ -367,7 +382,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                    b0 + (uint64_t)((ks / 4) * (kBoxBytes / 16) + (ks % 4) * 2),
                                    idesc_s, k > 0 ? 1u : 0u);
                     }
-                    if (!L::kReleaseByS) mma_commit(smem_u32(&bars.empty[slot]));
                 }
                 mma_commit(smem_u32(&bars.s_full[j & 3u]));
                 return true;
