@@ -6,8 +6,13 @@ Argument marshalling only: every step of the computation runs in the CUDA
 kernels of ``libattn.so``.  Tensors are torch CUDA tensors (fp32, 16-byte
 aligned); plain integers are accepted as raw device pointers.  The functions
 carry the C names and argument order; a workspace is allocated with torch
-when the caller passes none.  There is no CPU fallback: importing this
-package fails loudly when the library has not been built.
+when the caller passes none.  The five calls that launch kernels convert
+their arguments in the small C extension ``_calls`` (a decode step is a few
+microseconds of GPU work, and ctypes' per-argument conversion is a visible
+part of that on the host); sizes must be non-negative and below 2^32.  The
+other calls go through ctypes.  ``lib`` stays available for direct ctypes
+calls.  There is no CPU fallback: importing this package fails loudly when
+the library or the extension has not been built.
 """
 from __future__ import annotations
 
@@ -63,6 +68,16 @@ for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
     _fn.restype, _fn.argtypes = _res, _args
 
+try:
+    from . import _calls
+except ImportError as _e:
+    raise ImportError(
+        f"the _calls extension is not built next to {library_path} ({_e}); run "
+        "`python -c 'import __graft_entry__ as g; g.build()'` first") from _e
+_calls.bind(*(ctypes.cast(getattr(lib, _n), ctypes.c_void_p).value
+              for _n in ("attn_prefill_causal", "attn_decode", "attn_decode_append",
+                         "attn_decode_noalloc", "kv_append")))
+
 
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -78,21 +93,9 @@ def exported_symbols() -> list[str]:
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?([a-z_0-9]+)\(", text, re.M)))
 
 
-def _ptr(x):
-    if x is None:
-        return None
-    if isinstance(x, int):
-        return x
-    return x.data_ptr()
-
-
-def _stream(stream):
-    if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
-    if isinstance(stream, int):
-        return stream
-    return stream.cuda_stream
+def _current_stream():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _check(status: int, where: str, check: bool) -> int:
@@ -140,12 +143,14 @@ def attn_prefill_causal(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_st
                         stream=None, check=True):
     """Causal GQA prefill (C: attn_prefill_causal).  q/o: [m, q_stride] fp32,
     k/v: [m, kv_stride] fp32.  Returns the status (raises when ``check``)."""
-    workspace, workspace_bytes = _workspace_args(
-        workspace, workspace_bytes,
-        lambda: attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim, precision), q)
-    st = lib.attn_prefill_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(o), m, num_q_heads, num_kv_heads,
-                                 head_dim, q_stride, kv_stride, float(scale), int(precision),
-                                 _ptr(workspace), workspace_bytes, _stream(stream))
+    if workspace is None or workspace_bytes is None:
+        workspace, workspace_bytes = _workspace_args(
+            workspace, workspace_bytes,
+            lambda: attn_prefill_workspace_size(m, num_q_heads, num_kv_heads, head_dim,
+                                                precision), q)
+    st = _calls.attn_prefill_causal(q, k, v, o, m, num_q_heads, num_kv_heads, head_dim, q_stride,
+                                    kv_stride, scale, precision, workspace, workspace_bytes,
+                                    _current_stream() if stream is None else stream)
     return _check(st, "attn_prefill_causal", check)
 
 
@@ -153,13 +158,14 @@ def attn_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq
                 window=0, scale=0.0, workspace=None, workspace_bytes=None, stream=None, check=True):
     """Single-query GQA decode (C: attn_decode).  q/out: [num_heads, head_dim];
     caches: [kv_heads, max_seq, head_dim].  Returns the status."""
-    workspace, workspace_bytes = _workspace_args(
-        workspace, workspace_bytes,
-        lambda: attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window),
-        k_cache)
-    st = lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, kv_heads,
-                         head_dim, max_seq, total_seq, window, float(scale), _ptr(workspace),
-                         workspace_bytes, _stream(stream))
+    if workspace is None or workspace_bytes is None:
+        workspace, workspace_bytes = _workspace_args(
+            workspace, workspace_bytes,
+            lambda: attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window),
+            k_cache)
+    st = _calls.attn_decode(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim, max_seq,
+                            total_seq, window, scale, workspace, workspace_bytes,
+                            _current_stream() if stream is None else stream)
     return _check(st, "attn_decode", check)
 
 
@@ -168,14 +174,15 @@ def attn_decode_append(q, k_new, v_new, k_cache, v_cache, out, num_heads, kv_hea
                        rope_sin=None, workspace=None, workspace_bytes=None, stream=None,
                        check=True):
     """Fused (RoPE +) append + decode (C: attn_decode_append)."""
-    workspace, workspace_bytes = _workspace_args(
-        workspace, workspace_bytes,
-        lambda: attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window),
-        k_cache)
-    st = lib.attn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(rope_cos), _ptr(rope_sin),
-                                _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, kv_heads,
-                                head_dim, max_seq, total_seq, position, window, float(scale),
-                                _ptr(workspace), workspace_bytes, _stream(stream))
+    if workspace is None or workspace_bytes is None:
+        workspace, workspace_bytes = _workspace_args(
+            workspace, workspace_bytes,
+            lambda: attn_decode_workspace_size(num_heads, kv_heads, head_dim, total_seq, window),
+            k_cache)
+    st = _calls.attn_decode_append(q, k_new, v_new, rope_cos, rope_sin, k_cache, v_cache, out,
+                                   num_heads, kv_heads, head_dim, max_seq, total_seq, position,
+                                   window, scale, workspace, workspace_bytes,
+                                   _current_stream() if stream is None else stream)
     return _check(st, "attn_decode_append", check)
 
 
@@ -183,17 +190,17 @@ def attn_decode_noalloc(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim,
                         total_seq, window=0, scale=0.0, stream=None, check=True):
     """attn_decode with the library's fixed scratch instead of a workspace
     (C: attn_decode_noalloc).  For callers that cannot allocate."""
-    st = lib.attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads,
-                                 kv_heads, head_dim, max_seq, total_seq, window, float(scale),
-                                 _stream(stream))
+    st = _calls.attn_decode_noalloc(q, k_cache, v_cache, out, num_heads, kv_heads, head_dim,
+                                    max_seq, total_seq, window, scale,
+                                    _current_stream() if stream is None else stream)
     return _check(st, "attn_decode_noalloc", check)
 
 
 def kv_append(k_src, v_src, k_cache, v_cache, kv_heads, head_dim, max_seq, position, stream=None,
               check=True):
     """Write one K row and one V row at ``position`` (C: kv_append)."""
-    st = lib.kv_append(_ptr(k_src), _ptr(v_src), _ptr(k_cache), _ptr(v_cache), kv_heads, head_dim,
-                       max_seq, position, _stream(stream))
+    st = _calls.kv_append(k_src, v_src, k_cache, v_cache, kv_heads, head_dim, max_seq, position,
+                          _current_stream() if stream is None else stream)
     return _check(st, "kv_append", check)
 
 

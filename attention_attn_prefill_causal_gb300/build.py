@@ -1,9 +1,12 @@
-"""Build libattn.so in-tree with nvcc for sm_103a (no cmake, no torch).
+"""Build libattn.so in-tree with nvcc for sm_103a (no cmake, no torch), and
+the CPython extension `_calls` (csrc/pycalls.c) with the host C compiler.
 
 Each .cu under csrc/ compiles to an object in parallel; the objects link into
 attention_attn_prefill_causal_gb300/libattn.so with the CUDA runtime linked
 statically, so the library loads on a machine without a GPU driver (the
-driver is only needed when a call reaches the device).
+driver is only needed when a call reaches the device).  `_calls` is not
+linked against libattn.so: the package hands it the library's function
+addresses at import.
 """
 from __future__ import annotations
 
@@ -13,6 +16,7 @@ import os
 import shutil
 import subprocess
 import sys
+import sysconfig
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
@@ -31,9 +35,41 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libattn")
 
 
+PYCALLS_SRC = os.path.join(CSRC, "pycalls.c")
+PYCALLS = os.path.join(PKG, "_calls" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+
+
 def _deps_mtime() -> float:
-    files = glob.glob(os.path.join(CSRC, "*")) + [os.path.join(ROOT, "include", "attn.h")]
+    files = [f for f in glob.glob(os.path.join(CSRC, "*")) if f != PYCALLS_SRC]
+    files.append(os.path.join(ROOT, "include", "attn.h"))
     return max(os.path.getmtime(f) for f in files)
+
+
+def _host_cc() -> str:
+    for c in (os.environ.get("CC"), shutil.which("gcc"), shutil.which("cc")):
+        if c and (os.path.exists(c) or shutil.which(c)):
+            return c
+    raise RuntimeError("no host C compiler (gcc) found: it builds the _calls extension")
+
+
+def build_pycalls(force: bool = False) -> str:
+    """Compile the _calls extension if its source or the header is newer."""
+    hdr = os.path.join(ROOT, "include", "attn.h")
+    if (not force and os.path.exists(PYCALLS)
+            and os.path.getmtime(PYCALLS) >= max(os.path.getmtime(PYCALLS_SRC),
+                                                 os.path.getmtime(hdr))):
+        return PYCALLS
+    inc = sysconfig.get_paths()["include"]
+    if not os.path.exists(os.path.join(inc, "Python.h")):
+        raise RuntimeError(f"Python.h not found in {inc}: it builds the _calls extension")
+    tmp = PYCALLS + f".tmp{os.getpid()}"
+    cmd = [_host_cc(), "-O2", "-shared", "-fPIC", "-Wall", "-I", inc, PYCALLS_SRC,
+           "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"building _calls failed:\n{r.stdout}{r.stderr}")
+    os.replace(tmp, PYCALLS)
+    return PYCALLS
 
 
 def _compile(src: str, verbose: bool) -> tuple[str, str]:
@@ -51,8 +87,10 @@ def _compile(src: str, verbose: bool) -> tuple[str, str]:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libattn.so if any source is newer than it."""
+    """Compile and link libattn.so if any source is newer than it, and the
+    _calls extension likewise."""
     os.makedirs(BUILD, exist_ok=True)
+    build_pycalls(force)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
         return LIB
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
