@@ -411,8 +411,16 @@ class PrefillBench:
         # every row of a short prompt; a seeded sample of rows of a long one
         # (the full comparison of the long prompt is a GPU test of its own)
         rows = None if c.m <= 4096 else workloads.sample_rows(c.m, c.seed, 16, 16, 32)
+        t0 = time.perf_counter()
         ref = oracle.prefill_causal(q.numpy(), k.numpy(), v.numpy(), c.m, c.num_q_heads,
                                     c.num_kv_heads, c.head_dim, c.q_stride, c.kv_stride, rows=rows)
+        secs = time.perf_counter() - t0
+        # the oracle's own rate on the host cores: row i attends i + 1 keys,
+        # 4 * head_dim FLOP per key and query head (scores and P.V)
+        keys = c.m * (c.m + 1) // 2 if rows is None else int(sum(int(r) + 1 for r in rows))
+        self.oracle_tflops = 4.0 * c.head_dim * c.num_q_heads * keys / secs / 1e12
+        self.oracle_rows = c.m if rows is None else len(rows)
+        self.oracle_cores = oracle.max_threads()
         self.call(0, torch.cuda.current_stream())
         torch.cuda.synchronize()
         got = self.o[0].view(c.m, c.q_stride)[:, : c.num_q_heads * c.head_dim]
@@ -563,6 +571,7 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
     compact = {"value": round(tflops, 2), "unit": "TFLOP/s", "us": round(per_call * 1e6, 2),
                "frac": round(tflops / peak, 4), "err": float(f"{err:.3g}"),
                "e2e": round(flops / e2e_per_call / 1e12, 2),
+               "cpu": float(f"{pb.oracle_tflops:.3g}"),
                "launches": pb.launches_per_call}
     detail = {"workload": shape.name, "calls": n, "flops_per_call": flops,
               "peak": peak, "peak_source": f"{peak_key} ({peak_src})", "kernel": kname,
@@ -570,7 +579,9 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
               "l2": (f"inputs {pb.R} rotating replicas" if pb.R > 1 else "inputs larger than 2x L2"),
               "e2e_pipelined_ms": round(e2e_per_call * 1e3, 4),
               "e2e_serial_ms": round(serial_per_call * 1e3, 4),
-              "e2e_calls": e_calls, "h2d_bytes_per_call": h2d, "d2h_bytes_per_call": d2h}
+              "e2e_calls": e_calls, "h2d_bytes_per_call": h2d, "d2h_bytes_per_call": d2h,
+              "cpu_oracle": {"tflops": pb.oracle_tflops, "rows": pb.oracle_rows,
+                             "cores": pb.oracle_cores}}
     return compact, detail
 
 

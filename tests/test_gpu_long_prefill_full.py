@@ -2,7 +2,7 @@
 over 4 KV heads, head_dim 128, packed strides 3584 / 512, N(0,1) inputs
 scaled by 0.5 from seed 4): every one of the 58.7 M outputs of each precision
 mode is compared with the fp64 oracle, which runs once for the module (about
-two minutes of OpenMP work on 16 host cores).
+35 s of OpenMP work on 16 host cores).
 
 Tolerances: max abs <= 1e-4 and normwise relative <= 1e-4 for the exact fp32
 mode; max abs <= 3e-3 for the tensor-core modes.  Outputs are NaN-poisoned
