@@ -571,7 +571,7 @@ def bench_prefill(attn, shape, device, stream, calls, peaks, peak_src):
     compact = {"value": round(tflops, 2), "unit": "TFLOP/s", "us": round(per_call * 1e6, 2),
                "frac": round(tflops / peak, 4), "err": float(f"{err:.3g}"),
                "e2e": round(flops / e2e_per_call / 1e12, 2),
-               "cpu": float(f"{pb.oracle_tflops:.3g}"),
+               "cpu": float(f"{pb.oracle_tflops:.3g}"), "traffic": traffic,
                "launches": pb.launches_per_call}
     detail = {"workload": shape.name, "calls": n, "flops_per_call": flops,
               "peak": peak, "peak_source": f"{peak_key} ({peak_src})", "kernel": kname,
@@ -635,8 +635,9 @@ def bench_decode_companion(attn, shape, device, stream, steps, peaks, peak_src):
     live = shape.kv_bytes_algorithmic()
     hbm = float(peaks["hbm_gbs"])
     gbs = live / per / 1e9
+    traffic = traffic_for(f"attn_decode:{shape.name}", ["decode.cu"])
     compact = {"value": round(gbs, 2), "unit": "GB/s", "us": round(per * 1e6, 3),
-               "frac": round(gbs / hbm, 4), "err": float(f"{err:.3g}")}
+               "frac": round(gbs / hbm, 4), "err": float(f"{err:.3g}"), "traffic": traffic}
     if shape.window:
         compact["copy_floor_us"] = round(copy_floor_us(db.kc, live, stream), 3)
         # the same time over the formula's byte count (all total_seq rows,
@@ -646,7 +647,7 @@ def bench_decode_companion(attn, shape, device, stream, steps, peaks, peak_src):
               "bytes_all_rows": shape.kv_bytes_all_rows(),
               "gbs_all_rows_formula": round(shape.kv_bytes_all_rows() / per / 1e9, 2),
               "l2": f"{db.R} rotating cache replicas (live bytes {db.R * live // 2**20} MiB)",
-              "traffic": traffic_for(f"attn_decode:{shape.name}", ["decode.cu"]),
+              "traffic": traffic,
               "peak_source": f"hbm_gbs ({peak_src})", "launches_per_step": db.launches_per_step}
     return compact, detail
 
