@@ -57,6 +57,12 @@ MUTANTS = {
                                    "const float *kb = k_cache + (size_t)kvh * total_seq * d;"),
     "rope_cos_sin_swapped": ("const double c = (double)cosv[i], sn = (double)sinv[i];",
                              "const double c = (double)sinv[i], sn = (double)cosv[i];"),
+    "append_value_from_key": ("if (v_cache) v_cache[dst] = v_src[src];",
+                              "if (v_cache) v_cache[dst] = k_src[src];"),
+    "fused_key_not_rotated": ("if (rope_cos) rope(tmp, rope_cos, rope_sin, d, tmp + d);",
+                              "if (0) rope(tmp, rope_cos, rope_sin, d, tmp + d);"),
+    "prefill_scale_squared": ("s[j] = scale * dot;", "s[j] = scale * scale * dot;"),
+    "window_start_from_max_seq": ("total_seq - window : 0;", "max_seq - window : 0;"),
 }
 
 
