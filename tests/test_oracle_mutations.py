@@ -63,6 +63,12 @@ MUTANTS = {
                               "if (0) rope(tmp, rope_cos, rope_sin, d, tmp + d);"),
     "prefill_scale_squared": ("s[j] = scale * dot;", "s[j] = scale * scale * dot;"),
     "window_start_from_max_seq": ("total_seq - window : 0;", "max_seq - window : 0;"),
+    "decode_query_is_kv_head": ("const double *qh = qd + (size_t)h * d;",
+                                "const double *qh = qd + (size_t)kvh * d;"),
+    "decode_value_from_key_cache": ("const float *vb = v_cache + (size_t)kvh * max_seq * d;",
+                                    "const float *vb = k_cache + (size_t)kvh * max_seq * d;"),
+    "window_masks_newest_rows": ("if (t < ws) s[t] = -1.0e4;",
+                                 "if (t >= total_seq - ws) s[t] = -1.0e4;"),
 }
 
 
